@@ -1,0 +1,214 @@
+/*
+ * nomas.h - C ABI of the segment-causal KV-cache attention library (B300, sm_103a).
+ *
+ * The library implements the per-block hot path of a segment-autoregressive
+ * video diffusion transformer of the Hy-Nomas kind: each segment's video and
+ * text queries attend over a persistent KV cache of earlier latent frames plus
+ * the segment's own keys and values ("segment-wise causal joint attention", the
+ * madebyagents.com model page; the lifelong KV cache of the orcarouter.ai
+ * explainer, section "Die Schleife"), with 3D rotary positions and an optional
+ * INT8, sliding-window cache (the low-memory preset of "Hy-Nomas auf einer RTX
+ * 4090", section "Das Single-GPU-Preset": kv_cache_quantization int8,
+ * past_frames 18).
+ *
+ * Conventions (all entry points):
+ *  - Every device pointer is caller-owned device memory; the library never
+ *    allocates, frees or synchronises.  Work is enqueued on the given stream
+ *    and runs asynchronously; host-side metadata is updated at enqueue time.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failed validation returns a status and launches nothing.  A CUDA launch
+ *    error returns NOMAS_ERR_CUDA.
+ *  - Shapes: head_dim must be 128.  Activations are token-major
+ *    [tokens][heads][head_dim] with the heads of a token contiguous.  Video
+ *    tokens come first, in (latent frame, h, w) row-major order, then text
+ *    tokens.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Calls on distinct cache descriptors are thread-safe.
+ *  - Kernels that wait on on-chip barriers give up after about one second,
+ *    record NOMAS_ERR_DEVICE_TIMEOUT in a device-side error word and return;
+ *    nomas_device_error() reads and optionally clears that word.
+ */
+#ifndef NOMAS_H_
+#define NOMAS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NOMAS_OK = 0,
+  NOMAS_ERR_INVALID_ARG = 1,    /* bad pointer, shape, dtype, alignment or scale   */
+  NOMAS_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. head_dim != 128) */
+  NOMAS_ERR_CAPACITY = 3,       /* append beyond the capacity of a cache w/o window */
+  NOMAS_ERR_CUDA = 4,           /* a CUDA runtime / launch error                    */
+  NOMAS_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up waiting on an on-chip barrier   */
+} nomas_status;
+
+typedef enum { NOMAS_F32 = 0, NOMAS_BF16 = 1, NOMAS_INT8 = 2 } nomas_dtype;
+
+/*
+ * Persistent KV cache of num_blocks transformer blocks (the lifelong cache of
+ * the orcarouter.ai explainer, section "Die Schleife"; windowed per "Das
+ * Single-GPU-Preset" of the inferencekey.com RTX 4090 test).
+ *
+ * Layout (caller-allocated device memory):
+ *   k, v       [num_blocks][heads][capacity_frames * grid_h * grid_w][head_dim]
+ *              int8 codes (dtype NOMAS_INT8) or bf16 values (NOMAS_BF16)
+ *   k_scale,   [num_blocks][heads][capacity_frames * grid_h * grid_w] float32,
+ *   v_scale    one scale per (block, head, token); NULL for NOMAS_BF16
+ * Absolute latent frame f lives in frame-slot (f mod capacity_frames); token
+ * (h, w) of that frame sits at slot (f mod capacity_frames)*grid_h*grid_w +
+ * h*grid_w + w.  Resident slots are always [0, valid_frames*grid_h*grid_w).
+ * INT8 codes: scale = fl32(absmax/127), code = clamp(rint(fl32(x *
+ * fl32(127/absmax))), -127, 127), ties to even; an all-zero row has scale 0.
+ *
+ * past_frames > 0 is a sliding window of that many latent frames and requires
+ * capacity_frames == past_frames; past_frames == 0 means no window (appending
+ * beyond capacity_frames is NOMAS_ERR_CAPACITY).  total_frames and
+ * valid_frames are host metadata maintained by append and reset; a caller
+ * creating a descriptor sets them to 0.  Saving the struct and the device
+ * buffers and restoring both resumes a session.
+ */
+typedef struct {
+  int32_t num_blocks;      /* transformer blocks sharing this descriptor (>= 1)  */
+  int32_t heads;           /* attention heads (>= 1)                              */
+  int32_t head_dim;        /* must be 128                                         */
+  int32_t grid_h;          /* latent rows per frame                               */
+  int32_t grid_w;          /* latent columns per frame                            */
+  int32_t capacity_frames; /* ring size in latent frames                          */
+  int32_t past_frames;     /* window in latent frames; 0 = none                   */
+  int32_t dtype;           /* nomas_dtype: NOMAS_INT8 or NOMAS_BF16               */
+  void* k;                 /* device                                              */
+  void* v;                 /* device                                              */
+  float* k_scale;          /* device, INT8 only                                   */
+  float* v_scale;          /* device, INT8 only                                   */
+  int64_t total_frames;    /* absolute latent frames ever appended (host)         */
+  int32_t valid_frames;    /* resident frames = min(total_frames, window) (host)  */
+  int32_t reserved;        /* must be 0                                           */
+} nomas_kvcache;
+
+/* Library version (major*10000 + minor*100 + patch). Host only. */
+int32_t nomas_version(void);
+
+/* Human-readable name of a status. Host only; never NULL. */
+const char* nomas_status_string(nomas_status s);
+
+/* Check a descriptor's shape fields and pointers (no device access). */
+nomas_status nomas_kvcache_validate(const nomas_kvcache* cache);
+
+/* Device bytes the descriptor's k, v (and scales) need; 0 if invalid. Host only.
+ * INT8: 2 * blocks*heads*slots*(head_dim + 4); BF16: 2 * blocks*heads*slots*head_dim*2,
+ * slots = capacity_frames*grid_h*grid_w. */
+size_t nomas_kvcache_bytes(const nomas_kvcache* cache);
+
+/*
+ * What nomas_kvcache_append of n_frames would do, without doing it (host only).
+ * first_frame: the first frame of the new segment that is written (frames
+ * before it fall outside the window and are never written); slot_frame: the
+ * ring frame-slot it goes to; new_total / new_valid: metadata afterwards.
+ * Any output pointer may be NULL.  Returns NOMAS_ERR_CAPACITY when a cache
+ * without a window would overflow.
+ */
+nomas_status nomas_kvcache_plan_append(const nomas_kvcache* cache, int32_t n_frames,
+                                       int32_t* first_frame, int32_t* slot_frame,
+                                       int64_t* new_total, int32_t* new_valid);
+
+/*
+ * 3D rotary position embedding, in place, on the video rows of Q (and K).
+ * Model card: "3D RoPE" (inferencekey.com RTX 4090 test, "Modell und
+ * Dateien").  Reading: head_dim splits into d_t, d_h, d_w contiguous chunks
+ * (d_t + d_h + d_w <= head_dim, each even); inside the chunk of axis a, pair
+ * (x[o+2i], x[o+2i+1]) rotates by pos_a * theta^(-2i/d_a):
+ * (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos).  Video token n has positions
+ * (t0 + n / (grid_h*grid_w), (n mod grid_h*grid_w) / grid_w, n mod grid_w).
+ *
+ *   q, k              device, [n_video..][heads][head_dim] of io_dt (F32 or
+ *                     BF16), row stride row_stride_elems elements; rows
+ *                     [0, n_video) are rotated, nothing else is touched.
+ *                     k may be NULL.
+ *   n_video           must equal frames*grid_h*grid_w
+ *   t0                absolute latent frame of the segment's first frame
+ *   theta             frequency base (> 0), e.g. 10000
+ * Math in float32 (angles reduced with a compensated product), one rounding
+ * to io_dt at the end.
+ */
+nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, int32_t n_video,
+                                int32_t heads, int32_t head_dim, int64_t row_stride_elems,
+                                int32_t frames, int32_t grid_h, int32_t grid_w, int64_t t0,
+                                float theta, int32_t d_t, int32_t d_h, int32_t d_w,
+                                cudaStream_t stream);
+
+/*
+ * Append a finished segment's K/V for all blocks (the KV-cache write stage,
+ * "Zeiten" on the inferencekey.com RTX 4090 test page), quantising to INT8
+ * with per-(block, head, token) scales or copying to BF16, into the ring; frames
+ * older than the window are never written (a segment longer than the window
+ * writes only its last past_frames frames).  Updates cache->total_frames and
+ * cache->valid_frames after a successful enqueue.
+ *
+ *   k, v                device, [num_blocks][n_frames*grid_h*grid_w][heads][head_dim]
+ *                       of in_dt (F32 or BF16); block b starts at
+ *                       b*block_stride_elems elements
+ *   block_stride_elems  >= n_frames*grid_h*grid_w*heads*head_dim
+ */
+nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k, const void* v,
+                                  nomas_dtype in_dt, int32_t n_frames,
+                                  int64_t block_stride_elems, cudaStream_t stream);
+
+/*
+ * Scratch bytes nomas_segment_attn needs for a given split count (0 = the
+ * split count it would choose itself).  Host only.
+ */
+nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int32_t n_video,
+                                                int32_t n_text, int32_t num_splits,
+                                                size_t* bytes);
+
+/*
+ * Segment attention of one block (the "segment-wise causal joint attention"
+ * of the madebyagents.com model page over the lifelong cache of the
+ * orcarouter.ai explainer): per head, O = softmax(s * Q K^T) V over the keys
+ * [resident cache of `block` (dequantised if INT8) ; current segment's K/V],
+ * every current query seeing every key of that set.
+ *
+ *   q, k_cur, v_cur  device bf16 [n_video + n_text][heads][head_dim]
+ *   softmax_scale    s > 0 (1/sqrt(128) in the model)
+ *   out              device bf16 [n_video + n_text][heads][head_dim]
+ *   lse              device float32 [heads][n_video + n_text] (natural log), or NULL
+ *   workspace        device scratch of workspace_bytes (see
+ *                    nomas_segment_attn_workspace_bytes), or NULL/0: the key
+ *                    range is then processed in one split
+ *   num_splits       key-range splits (0 = automatic); more than 1 needs workspace
+ * BF16 tensor-core products with float32 accumulation and float32 softmax.
+ * Results are bitwise reproducible for a given split count.
+ */
+nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const void* q,
+                                const void* k_cur, const void* v_cur, int32_t n_video,
+                                int32_t n_text, float softmax_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, int32_t num_splits,
+                                cudaStream_t stream);
+
+/*
+ * Start a new session (the resident service's new session_id, "Setup" and the
+ * JSON turns on the inferencekey.com RTX 4090 test page): total_frames and
+ * valid_frames to 0; with zero_memory != 0 also enqueue a kernel that clears
+ * k, v and the scales.
+ */
+nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream);
+
+/*
+ * Read the device-side error word of the current device (a status code set
+ * by a kernel that gave up waiting, 0 if none), synchronously.  With clear != 0
+ * the word is reset to 0.  *status receives NOMAS_OK or the recorded status.
+ */
+nomas_status nomas_device_error(nomas_status* status, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NOMAS_H_ */

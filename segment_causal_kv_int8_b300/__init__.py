@@ -1,0 +1,256 @@
+"""Python binding of the segment-causal KV-cache attention library (``libnomas.so``).
+
+Argument marshalling only: every step of the hot path runs in the CUDA kernels
+behind the C ABI declared in ``include/nomas.h``.  PyTorch supplies device
+memory and streams.  The functions ``nomas_*`` mirror the C entry points one to
+one (ctypes); :class:`KVCache`, :func:`rope3d`, :func:`segment_attn` are thin
+conveniences over them that take torch tensors and raise :class:`NomasError`
+on any status other than ``NOMAS_OK``.
+
+There is no CPU fallback: importing this package loads the shared library and
+fails loudly when it has not been built (``python -m
+segment_causal_kv_int8_b300._build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnomas.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m segment_causal_kv_int8_b300._build` "
+        "(there is no fallback implementation)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------- enums
+NOMAS_OK = 0
+NOMAS_ERR_INVALID_ARG = 1
+NOMAS_ERR_UNSUPPORTED = 2
+NOMAS_ERR_CAPACITY = 3
+NOMAS_ERR_CUDA = 4
+NOMAS_ERR_DEVICE_TIMEOUT = 5
+
+NOMAS_F32 = 0
+NOMAS_BF16 = 1
+NOMAS_INT8 = 2
+
+
+class nomas_kvcache(ctypes.Structure):
+    """Mirror of the C ``nomas_kvcache`` descriptor."""
+
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("grid_h", ctypes.c_int32),
+        ("grid_w", ctypes.c_int32),
+        ("capacity_frames", ctypes.c_int32),
+        ("past_frames", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
+        ("total_frames", ctypes.c_int64),
+        ("valid_frames", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+_P = ctypes.POINTER
+_c_int, _i32, _i64, _f32, _vp, _sz = (ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                      ctypes.c_void_p, ctypes.c_size_t)
+
+# name -> (restype, argtypes); the declarations of include/nomas.h
+EXPORTS = {
+    "nomas_version": (_i32, []),
+    "nomas_status_string": (ctypes.c_char_p, [_c_int]),
+    "nomas_kvcache_validate": (_c_int, [_P(nomas_kvcache)]),
+    "nomas_kvcache_bytes": (_sz, [_P(nomas_kvcache)]),
+    "nomas_kvcache_plan_append": (_c_int, [_P(nomas_kvcache), _i32, _P(_i32), _P(_i32), _P(_i64), _P(_i32)]),
+    "nomas_rope3d_apply": (_c_int, [_vp, _vp, _c_int, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i64, _f32,
+                                    _i32, _i32, _i32, _vp]),
+    "nomas_kvcache_append": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _vp]),
+    "nomas_segment_attn_workspace_bytes": (_c_int, [_P(nomas_kvcache), _i32, _i32, _i32, _P(_sz)]),
+    "nomas_segment_attn": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
+                                    _sz, _i32, _vp]),
+    "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
+    "nomas_device_error": (_c_int, [_P(_c_int), _c_int]),
+}
+
+for _name, (_res, _args) in EXPORTS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+    globals()[_name] = _fn
+
+
+class NomasError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {nomas_status_string(status).decode()}")
+
+
+def _check(status: int, what: str) -> None:
+    if status != NOMAS_OK:
+        raise NomasError(status, what)
+
+
+# ---------------------------------------------------------------- torch conveniences
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return NOMAS_F32
+    if t.dtype == torch.bfloat16:
+        return NOMAS_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def rope3d(q, k, frames: int, grid_h: int, grid_w: int, t0: int, theta: float = 10000.0,
+           split=(32, 48, 48), stream=None) -> None:
+    """In-place 3D RoPE on the first ``frames * grid_h * grid_w`` rows of q (and k).
+
+    ``q``/``k``: CUDA tensors ``[tokens][heads][128]`` (float32 or bfloat16),
+    token rows contiguous; ``k`` may be None.
+    """
+    if not q.is_cuda or (k is not None and (not k.is_cuda or k.dtype != q.dtype or k.shape != q.shape)):
+        raise ValueError("q and k must be CUDA tensors of the same dtype and shape")
+    if q.dim() != 3 or q.stride(2) != 1 or q.stride(1) != q.shape[2] or (k is not None and k.stride() != q.stride()):
+        raise ValueError("expected [tokens][heads][head_dim] with contiguous heads")
+    n_video = frames * grid_h * grid_w
+    _check(nomas_rope3d_apply(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr() if k is not None else 0),
+                              _dt_code(q), n_video, q.shape[1], q.shape[2], q.stride(0), frames, grid_h, grid_w,
+                              t0, theta, split[0], split[1], split[2], _stream_ptr(stream)), "nomas_rope3d_apply")
+
+
+class KVCache:
+    """A persistent ring KV cache whose device buffers are torch tensors.
+
+    ``dtype``: "int8" (codes + float32 per-(block, head, token) scales) or "bf16".
+    """
+
+    def __init__(self, num_blocks: int, heads: int, grid_h: int, grid_w: int, capacity_frames: int,
+                 past_frames: int = 0, dtype: str = "int8", device="cuda", head_dim: int = 128):
+        torch = _torch()
+        slots = capacity_frames * grid_h * grid_w
+        shape = (num_blocks, heads, slots, head_dim)
+        if dtype == "int8":
+            self.k = torch.zeros(shape, dtype=torch.int8, device=device)
+            self.v = torch.zeros(shape, dtype=torch.int8, device=device)
+            self.k_scale = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+            self.v_scale = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+            code = NOMAS_INT8
+        elif dtype == "bf16":
+            self.k = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+            self.v = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+            self.k_scale = self.v_scale = None
+            code = NOMAS_BF16
+        else:
+            raise ValueError("dtype must be 'int8' or 'bf16'")
+        self.dtype = dtype
+        self.desc = nomas_kvcache(num_blocks, heads, head_dim, grid_h, grid_w, capacity_frames, past_frames, code,
+                                  self.k.data_ptr(), self.v.data_ptr(),
+                                  self.k_scale.data_ptr() if self.k_scale is not None else None,
+                                  self.v_scale.data_ptr() if self.v_scale is not None else None, 0, 0, 0)
+        _check(nomas_kvcache_validate(ctypes.byref(self.desc)), "nomas_kvcache_validate")
+
+    @property
+    def total_frames(self) -> int:
+        return int(self.desc.total_frames)
+
+    @property
+    def valid_frames(self) -> int:
+        return int(self.desc.valid_frames)
+
+    @property
+    def tpf(self) -> int:
+        return self.desc.grid_h * self.desc.grid_w
+
+    def nbytes(self) -> int:
+        return int(nomas_kvcache_bytes(ctypes.byref(self.desc)))
+
+    def append(self, k, v, stream=None) -> None:
+        """Append a finished segment: ``k``, ``v`` ``[blocks][F*tpf][heads][128]`` (or 3-D for one block)."""
+        if k.dim() == 3:
+            k, v = k.unsqueeze(0), v.unsqueeze(0)
+        if k.shape != v.shape or k.dtype != v.dtype or not k.is_cuda:
+            raise ValueError("k and v must be CUDA tensors of equal shape and dtype")
+        if k.shape[0] != self.desc.num_blocks or k.shape[2] != self.desc.heads or k.shape[3] != self.desc.head_dim:
+            raise ValueError("K/V shape does not match the cache")
+        if k.shape[1] % self.tpf:
+            raise ValueError("token count is not a whole number of frames")
+        for t in (k, v):
+            if t.stride(3) != 1 or t.stride(2) != t.shape[3] or t.stride(1) != t.shape[2] * t.shape[3]:
+                raise ValueError("K/V rows must be contiguous within a block")
+        if k.stride() != v.stride():
+            raise ValueError("k and v must share strides")
+        _check(nomas_kvcache_append(ctypes.byref(self.desc), ctypes.c_void_p(k.data_ptr()),
+                                    ctypes.c_void_p(v.data_ptr()), _dt_code(k), k.shape[1] // self.tpf,
+                                    k.stride(0), _stream_ptr(stream)), "nomas_kvcache_append")
+
+    def reset(self, zero_memory: bool = False, stream=None) -> None:
+        _check(nomas_kvcache_reset(ctypes.byref(self.desc), int(bool(zero_memory)), _stream_ptr(stream)),
+               "nomas_kvcache_reset")
+
+    def workspace_bytes(self, n_video: int, n_text: int, num_splits: int = 0) -> int:
+        out = ctypes.c_size_t(0)
+        _check(nomas_segment_attn_workspace_bytes(ctypes.byref(self.desc), n_video, n_text, num_splits,
+                                                  ctypes.byref(out)), "nomas_segment_attn_workspace_bytes")
+        return int(out.value)
+
+
+def segment_attn(cache: KVCache, block: int, q, k_cur, v_cur, n_video: int, n_text: int,
+                 softmax_scale: Optional[float] = None, out=None, lse=None, workspace=None,
+                 num_splits: int = 0, stream=None):
+    """Segment attention of one block; returns ``out`` (bf16 ``[Nq][heads][128]``).
+
+    ``workspace``: optional CUDA uint8 tensor (see :meth:`KVCache.workspace_bytes`).
+    """
+    torch = _torch()
+    for t in (q, k_cur, v_cur):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k_cur, v_cur must be contiguous bfloat16 CUDA tensors")
+    nq = n_video + n_text
+    if q.shape[0] != nq or q.shape != k_cur.shape or q.shape != v_cur.shape:
+        raise ValueError("q/k_cur/v_cur must be [n_video + n_text][heads][128]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[2])
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(nomas_segment_attn(ctypes.byref(cache.desc), block, ctypes.c_void_p(q.data_ptr()),
+                              ctypes.c_void_p(k_cur.data_ptr()), ctypes.c_void_p(v_cur.data_ptr()), n_video, n_text,
+                              softmax_scale, ctypes.c_void_p(out.data_ptr()),
+                              ctypes.c_void_p(lse.data_ptr() if lse is not None else 0), ctypes.c_void_p(ws_ptr),
+                              ws_bytes, num_splits, _stream_ptr(stream)), "nomas_segment_attn")
+    return out
+
+
+def device_error(clear: bool = True) -> int:
+    """The device-side error word (0 = none), read synchronously."""
+    st = ctypes.c_int(0)
+    _check(nomas_device_error(ctypes.byref(st), int(bool(clear))), "nomas_device_error")
+    return int(st.value)
+
+
+__all__ = ["KVCache", "rope3d", "segment_attn", "device_error", "NomasError", "nomas_kvcache", "EXPORTS",
+           "LIB_PATH"] + list(EXPORTS)

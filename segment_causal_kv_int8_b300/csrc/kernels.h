@@ -1,0 +1,81 @@
+// kernels.h - internal interface between the C ABI shim and the CUDA kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nomas {
+
+// ------------------------------------------------------------------ RoPE-3D
+constexpr int kRopeMaxPairs = 64;  // head_dim 128 -> 64 rotary pairs
+
+struct RopeParams {
+  float f_hi[kRopeMaxPairs];     // frequency of each pair, high float
+  float f_lo[kRopeMaxPairs];     // fl32(f - f_hi): low float of a two-float frequency
+  int8_t axis[kRopeMaxPairs];    // 0 = t, 1 = h, 2 = w, -1 = not rotated
+  int n_video;
+  int heads;
+  long long row_stride;          // elements between tokens
+  int tpf;                       // grid_h * grid_w
+  int grid_w;
+  long long t0;
+};
+
+cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ append
+struct AppendParams {
+  const void* k;
+  const void* v;
+  long long block_stride;        // elements between blocks of the input
+  int blocks;
+  int heads;
+  int tpf;
+  int first_frame;               // first segment frame written
+  int n_tokens;                  // tokens written = (n_frames - first_frame) * tpf
+  long long total_before;        // absolute frames appended before this call
+  int capacity_frames;
+  long long cap_slots;           // capacity_frames * tpf
+  void* ck;                      // cache K (int8 or bf16)
+  void* cv;
+  float* ks;                     // scales (int8 only)
+  float* vs;
+};
+
+cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ reset
+cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);
+
+// ------------------------------------------------------------------ attention
+struct AttnTensorMaps {
+  CUtensorMap q, kcur, vcur, kc, vc;
+};
+
+struct AttnParams {
+  int nq;                        // current-segment tokens (queries and current keys)
+  int nc;                        // resident cache tokens
+  int heads;
+  int n_cache_tiles;             // ceil(nc / 128)
+  int n_cur_tiles;               // ceil(nq / 128)
+  int num_splits;
+  int block_head_base;           // block * heads: row of the cache's [blocks*heads] axis
+  float scale_log2;              // softmax scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;                    // nullable
+  float* ws_o;                   // [splits][heads][nq][128] f32 (splits > 1)
+  float* ws_lse;                 // [splits][heads][nq]
+  const float* k_scale;          // int8 cache scales, [blocks*heads][scale_stride]
+  const float* v_scale;
+  long long scale_stride;        // cache slots per (block, head)
+  uint32_t* err;                 // device error word
+};
+
+cudaError_t launch_segment_attn(bool int8_cache, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
+                                cudaStream_t stream);
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
+int attn_smem_bytes(bool int8_cache);
+
+}  // namespace nomas

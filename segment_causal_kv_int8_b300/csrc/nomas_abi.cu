@@ -1,0 +1,425 @@
+// nomas_abi.cu - the C ABI (include/nomas.h): argument validation, cache
+// metadata, TMA descriptor encoding and kernel launches.  Host code only; no
+// allocation, no synchronisation (except nomas_device_error, documented as
+// synchronous).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/nomas.h"
+#include "kernels.h"
+
+#define NOMAS_API extern "C" __attribute__((visibility("default")))
+
+namespace nomas {
+namespace {
+
+// Device-side error word: kernels that give up waiting store a status here.
+__device__ uint32_t g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {nullptr};
+int g_sm_count[kMaxDevices] = {0};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+nomas_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NOMAS_OK : NOMAS_ERR_CUDA; }
+
+// Per-device state (error word address, SM count), set up on first use.
+nomas_status device_state(uint32_t** err, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NOMAS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return NOMAS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return NOMAS_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return NOMAS_ERR_CUDA;
+    g_sm_count[dev] = n;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_sm_count[dev];
+  return NOMAS_OK;
+}
+
+nomas_status encoder(EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr)
+      return NOMAS_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  *fn = g_encode;
+  return NOMAS_OK;
+}
+
+int64_t window_of(const nomas_kvcache* c) { return c->past_frames > 0 ? c->past_frames : c->capacity_frames; }
+
+nomas_status validate_cache(const nomas_kvcache* c) {
+  if (c == nullptr) return NOMAS_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->heads <= 0 || c->grid_h <= 0 || c->grid_w <= 0 || c->capacity_frames <= 0 ||
+      c->past_frames < 0 || c->reserved != 0)
+    return NOMAS_ERR_INVALID_ARG;
+  if (c->head_dim <= 0) return NOMAS_ERR_INVALID_ARG;
+  if (c->head_dim != 128) return NOMAS_ERR_UNSUPPORTED;
+  if (c->past_frames > 0 && c->capacity_frames != c->past_frames) return NOMAS_ERR_INVALID_ARG;
+  if (c->dtype != NOMAS_INT8 && c->dtype != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
+  const int64_t tpf = static_cast<int64_t>(c->grid_h) * c->grid_w;
+  const int64_t slots = tpf * c->capacity_frames;
+  if (slots > (int64_t(1) << 30) || static_cast<int64_t>(c->num_blocks) * c->heads > (int64_t(1) << 24))
+    return NOMAS_ERR_UNSUPPORTED;
+  if (c->k == nullptr || c->v == nullptr || !aligned16(c->k) || !aligned16(c->v)) return NOMAS_ERR_INVALID_ARG;
+  if (c->dtype == NOMAS_INT8) {
+    if (c->k_scale == nullptr || c->v_scale == nullptr) return NOMAS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(c->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(c->v_scale) & 3u))
+      return NOMAS_ERR_INVALID_ARG;
+  }
+  if (c->total_frames < 0 || c->valid_frames < 0) return NOMAS_ERR_INVALID_ARG;
+  if (c->valid_frames != std::min<int64_t>(c->total_frames, window_of(c))) return NOMAS_ERR_INVALID_ARG;
+  return NOMAS_OK;
+}
+
+nomas_status plan(const nomas_kvcache* c, int32_t n_frames, int32_t* first, int32_t* slot_frame,
+                  int64_t* new_total, int32_t* new_valid) {
+  if (n_frames < 0) return NOMAS_ERR_INVALID_ARG;
+  const int64_t t = c->total_frames, w = window_of(c);
+  if (c->past_frames == 0 && t + n_frames > c->capacity_frames) return NOMAS_ERR_CAPACITY;
+  const int64_t f0 = std::max<int64_t>(0, n_frames - w);
+  if (first) *first = static_cast<int32_t>(f0);
+  if (slot_frame) *slot_frame = static_cast<int32_t>((t + f0) % c->capacity_frames);
+  if (new_total) *new_total = t + n_frames;
+  if (new_valid) *new_valid = static_cast<int32_t>(std::min<int64_t>(t + n_frames, w));
+  return NOMAS_OK;
+}
+
+// Encode a 3D tiled TMA descriptor (dims/strides innermost first, strides in bytes).
+nomas_status encode3d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn fn = nullptr;
+  nomas_status st = encoder(&fn);
+  if (st != NOMAS_OK) return st;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NOMAS_OK : NOMAS_ERR_CUDA;
+}
+
+struct AttnPlan {
+  int nq, nc, n_pairs, n_cache_tiles, n_cur_tiles, splits;
+  size_t ws_o_bytes, ws_lse_bytes;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int auto_splits(int units, int n_tiles, int heads, int nq, int sms) {
+  // Modelled time in units of one CTA tile-iteration (256 queries x 128 keys,
+  // about 1.1 us): waves x (tiles per split + fixed cost) plus, for splits > 1,
+  // the combine pass (write + read of f32 partials) at ~6.5 TB/s.
+  double best = 1e300;
+  int best_s = 1;
+  const int s_max = std::min(8, std::max(1, n_tiles / 4));
+  for (int s = 1; s <= s_max; ++s) {
+    const double waves = std::ceil(static_cast<double>(units) * s / sms);
+    double cost = waves * (std::ceil(static_cast<double>(n_tiles) / s) + 1.5);
+    if (s > 1) {
+      const double bytes = (2.0 * s + 0.5) * heads * static_cast<double>(nq) * 128 * 4;
+      cost += bytes / 6.5e12 / 1.1e-6;
+    }
+    if (cost < best * 0.98) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+AttnPlan attn_plan(const nomas_kvcache* c, int32_t n_video, int32_t n_text, int32_t num_splits, int sms) {
+  AttnPlan pl;
+  pl.nq = n_video + n_text;
+  pl.nc = static_cast<int>(static_cast<int64_t>(c->valid_frames) * c->grid_h * c->grid_w);
+  pl.n_pairs = (pl.nq + 255) / 256;
+  pl.n_cache_tiles = (pl.nc + 127) / 128;
+  pl.n_cur_tiles = (pl.nq + 127) / 128;
+  const int n_tiles = pl.n_cache_tiles + pl.n_cur_tiles;
+  int s = num_splits;
+  if (s <= 0) s = auto_splits(pl.n_pairs * c->heads, n_tiles, c->heads, pl.nq, sms > 0 ? sms : 148);
+  s = std::max(1, std::min(s, std::min(n_tiles, 64)));
+  pl.splits = s;
+  pl.ws_o_bytes = s > 1 ? round256(static_cast<size_t>(s) * c->heads * pl.nq * 128 * 4) : 0;
+  pl.ws_lse_bytes = s > 1 ? round256(static_cast<size_t>(s) * c->heads * pl.nq * 4) : 0;
+  return pl;
+}
+
+}  // namespace
+}  // namespace nomas
+
+using namespace nomas;
+
+NOMAS_API int32_t nomas_version(void) { return 100; }
+
+NOMAS_API const char* nomas_status_string(nomas_status s) {
+  switch (s) {
+    case NOMAS_OK: return "NOMAS_OK";
+    case NOMAS_ERR_INVALID_ARG: return "NOMAS_ERR_INVALID_ARG";
+    case NOMAS_ERR_UNSUPPORTED: return "NOMAS_ERR_UNSUPPORTED";
+    case NOMAS_ERR_CAPACITY: return "NOMAS_ERR_CAPACITY";
+    case NOMAS_ERR_CUDA: return "NOMAS_ERR_CUDA";
+    case NOMAS_ERR_DEVICE_TIMEOUT: return "NOMAS_ERR_DEVICE_TIMEOUT";
+  }
+  return "NOMAS_UNKNOWN_STATUS";
+}
+
+NOMAS_API nomas_status nomas_kvcache_validate(const nomas_kvcache* cache) { return validate_cache(cache); }
+
+NOMAS_API size_t nomas_kvcache_bytes(const nomas_kvcache* c) {
+  if (c == nullptr || c->num_blocks <= 0 || c->heads <= 0 || c->head_dim <= 0 || c->grid_h <= 0 || c->grid_w <= 0 ||
+      c->capacity_frames <= 0)
+    return 0;
+  const size_t rows = static_cast<size_t>(c->num_blocks) * c->heads * c->grid_h * c->grid_w * c->capacity_frames;
+  if (c->dtype == NOMAS_INT8) return 2 * rows * (static_cast<size_t>(c->head_dim) + 4);
+  if (c->dtype == NOMAS_BF16) return 2 * rows * static_cast<size_t>(c->head_dim) * 2;
+  return 0;
+}
+
+NOMAS_API nomas_status nomas_kvcache_plan_append(const nomas_kvcache* cache, int32_t n_frames, int32_t* first_frame,
+                                                 int32_t* slot_frame, int64_t* new_total, int32_t* new_valid) {
+  const nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  return plan(cache, n_frames, first_frame, slot_frame, new_total, new_valid);
+}
+
+NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, int32_t n_video, int32_t heads,
+                                          int32_t head_dim, int64_t row_stride_elems, int32_t frames, int32_t grid_h,
+                                          int32_t grid_w, int64_t t0, float theta, int32_t d_t, int32_t d_h,
+                                          int32_t d_w, cudaStream_t stream) {
+  if (io_dt != NOMAS_F32 && io_dt != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
+  if (q == nullptr || heads <= 0 || head_dim <= 0 || frames < 0 || grid_h <= 0 || grid_w <= 0 || n_video < 0)
+    return NOMAS_ERR_INVALID_ARG;
+  if (head_dim != 128) return NOMAS_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(frames) * grid_h * grid_w != n_video) return NOMAS_ERR_INVALID_ARG;
+  if (d_t < 0 || d_h < 0 || d_w < 0 || ((d_t | d_h | d_w) & 1) != 0 || d_t + d_h + d_w > head_dim)
+    return NOMAS_ERR_INVALID_ARG;
+  if (!(theta > 0.0f) || !isfinite(theta)) return NOMAS_ERR_INVALID_ARG;
+  if (t0 < 0 || t0 + frames >= (int64_t(1) << 24) || grid_h >= (1 << 24) || grid_w >= (1 << 24))
+    return NOMAS_ERR_UNSUPPORTED;
+  const int64_t esz = io_dt == NOMAS_BF16 ? 2 : 4;
+  if (row_stride_elems < static_cast<int64_t>(heads) * head_dim || (row_stride_elems * esz) % 16 != 0)
+    return NOMAS_ERR_INVALID_ARG;
+  if (!aligned16(q) || (k != nullptr && !aligned16(k))) return NOMAS_ERR_INVALID_ARG;
+  if (n_video == 0) return NOMAS_OK;
+  RopeParams p;
+  memset(&p, 0, sizeof(p));
+  const int dims[3] = {d_t, d_h, d_w};
+  int pair = 0;
+  for (int a = 0; a < 3; ++a) {
+    for (int i = 0; i < dims[a] / 2; ++i, ++pair) {
+      const double f = pow(static_cast<double>(theta), -2.0 * i / dims[a]);
+      p.f_hi[pair] = static_cast<float>(f);
+      p.f_lo[pair] = static_cast<float>(f - static_cast<double>(p.f_hi[pair]));
+      p.axis[pair] = static_cast<int8_t>(a);
+    }
+  }
+  for (; pair < kRopeMaxPairs; ++pair) p.axis[pair] = -1;
+  p.n_video = n_video;
+  p.heads = heads;
+  p.row_stride = row_stride_elems;
+  p.tpf = grid_h * grid_w;
+  p.grid_w = grid_w;
+  p.t0 = t0;
+  return from_cuda(launch_rope3d(io_dt == NOMAS_BF16, q, k, p, stream));
+}
+
+NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k, const void* v, nomas_dtype in_dt,
+                                            int32_t n_frames, int64_t block_stride_elems, cudaStream_t stream) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (in_dt != NOMAS_F32 && in_dt != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
+  if (n_frames < 0) return NOMAS_ERR_INVALID_ARG;
+  const int64_t tpf = static_cast<int64_t>(cache->grid_h) * cache->grid_w;
+  const int64_t seg_elems = n_frames * tpf * cache->heads * cache->head_dim;
+  if (n_frames > 0) {
+    if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return NOMAS_ERR_INVALID_ARG;
+    if (cache->num_blocks > 1 && block_stride_elems < seg_elems) return NOMAS_ERR_INVALID_ARG;
+    if (block_stride_elems < 0 || (block_stride_elems * (in_dt == NOMAS_F32 ? 4 : 2)) % 16 != 0)
+      return NOMAS_ERR_INVALID_ARG;
+  }
+  int32_t first = 0, slot_frame = 0, new_valid = 0;
+  int64_t new_total = 0;
+  st = plan(cache, n_frames, &first, &slot_frame, &new_total, &new_valid);
+  if (st != NOMAS_OK) return st;
+  const int64_t n_tokens = (n_frames - first) * tpf;
+  if (n_tokens > 0) {
+    if (n_tokens > (int64_t(1) << 30)) return NOMAS_ERR_UNSUPPORTED;
+    AppendParams p;
+    p.k = k;
+    p.v = v;
+    p.block_stride = block_stride_elems;
+    p.blocks = cache->num_blocks;
+    p.heads = cache->heads;
+    p.tpf = static_cast<int>(tpf);
+    p.first_frame = first;
+    p.n_tokens = static_cast<int>(n_tokens);
+    p.total_before = cache->total_frames;
+    p.capacity_frames = cache->capacity_frames;
+    p.cap_slots = tpf * cache->capacity_frames;
+    p.ck = cache->k;
+    p.cv = cache->v;
+    p.ks = cache->k_scale;
+    p.vs = cache->v_scale;
+    st = from_cuda(launch_append(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, stream));
+    if (st != NOMAS_OK) return st;
+  }
+  cache->total_frames = new_total;
+  cache->valid_frames = new_valid;
+  return NOMAS_OK;
+}
+
+NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (zero_memory) {
+    const size_t rows = static_cast<size_t>(cache->num_blocks) * cache->heads * cache->grid_h * cache->grid_w *
+                        cache->capacity_frames;
+    const size_t kv_bytes = rows * cache->head_dim * (cache->dtype == NOMAS_INT8 ? 1 : 2);
+    st = from_cuda(launch_zero_fill(cache->k, kv_bytes, stream));
+    if (st == NOMAS_OK) st = from_cuda(launch_zero_fill(cache->v, kv_bytes, stream));
+    if (st == NOMAS_OK && cache->dtype == NOMAS_INT8) {
+      st = from_cuda(launch_zero_fill(cache->k_scale, rows * 4, stream));
+      if (st == NOMAS_OK) st = from_cuda(launch_zero_fill(cache->v_scale, rows * 4, stream));
+    }
+    if (st != NOMAS_OK) return st;
+  }
+  cache->total_frames = 0;
+  cache->valid_frames = 0;
+  return NOMAS_OK;
+}
+
+NOMAS_API nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
+                                                          int32_t num_splits, size_t* bytes) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (bytes == nullptr || n_video < 0 || n_text < 0 || num_splits < 0) return NOMAS_ERR_INVALID_ARG;
+  int sms = 148;
+  if (num_splits == 0) {
+    // The automatic split count depends on the device's SM count.
+    if (device_state(nullptr, &sms) != NOMAS_OK) sms = 148;
+  }
+  const AttnPlan pl = attn_plan(cache, n_video, n_text, num_splits, sms);
+  *bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
+  return NOMAS_OK;
+}
+
+NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const void* q, const void* k_cur,
+                                          const void* v_cur, int32_t n_video, int32_t n_text, float softmax_scale,
+                                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                          int32_t num_splits, cudaStream_t stream) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (block < 0 || block >= cache->num_blocks || n_video < 0 || n_text < 0 || num_splits < 0)
+    return NOMAS_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || !isfinite(softmax_scale)) return NOMAS_ERR_INVALID_ARG;
+  if (q == nullptr || k_cur == nullptr || v_cur == nullptr || out == nullptr) return NOMAS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cur) || !aligned16(v_cur) || !aligned16(out)) return NOMAS_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return NOMAS_ERR_INVALID_ARG;
+  if (cache->heads > 65535) return NOMAS_ERR_UNSUPPORTED;
+  const int64_t nq64 = static_cast<int64_t>(n_video) + n_text;
+  if (nq64 == 0) return NOMAS_OK;
+  if (nq64 > (int64_t(1) << 28)) return NOMAS_ERR_UNSUPPORTED;
+  uint32_t* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != NOMAS_OK) return st;
+  AttnPlan pl = attn_plan(cache, n_video, n_text, num_splits, sms);
+  if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_o_bytes + pl.ws_lse_bytes ||
+                        (reinterpret_cast<uintptr_t>(workspace) & 255u))) {
+    if (num_splits > 1) return NOMAS_ERR_INVALID_ARG;  // an explicit split count needs its workspace
+    pl = attn_plan(cache, n_video, n_text, 1, sms);
+  }
+  const bool int8 = cache->dtype == NOMAS_INT8;
+  AttnTensorMaps tm;
+  memset(&tm, 0, sizeof(tm));
+  const uint64_t H = cache->heads;
+  const uint64_t tok_stride = H * 128 * 2;
+  st = encode3d(&tm.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(q), 128, H, pl.nq, 256, tok_stride, 64, 1,
+                128);
+  if (st == NOMAS_OK)
+    st = encode3d(&tm.kcur, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(k_cur), 128, H, pl.nq, 256,
+                  tok_stride, 64, 1, 128);
+  if (st == NOMAS_OK)
+    st = encode3d(&tm.vcur, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(v_cur), 128, H, pl.nq, 256,
+                  tok_stride, 64, 1, 128);
+  const uint64_t cap_slots = static_cast<uint64_t>(cache->grid_h) * cache->grid_w * cache->capacity_frames;
+  const uint64_t bh_rows = static_cast<uint64_t>(cache->num_blocks) * H;
+  if (st == NOMAS_OK && pl.nc > 0) {
+    if (int8) {
+      st = encode3d(&tm.kc, CU_TENSOR_MAP_DATA_TYPE_UINT8, cache->k, 128, pl.nc, bh_rows, 128, cap_slots * 128, 128,
+                    128, 1);
+      if (st == NOMAS_OK)
+        st = encode3d(&tm.vc, CU_TENSOR_MAP_DATA_TYPE_UINT8, cache->v, 128, pl.nc, bh_rows, 128, cap_slots * 128, 128,
+                      128, 1);
+    } else {
+      st = encode3d(&tm.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k, 128, pl.nc, bh_rows, 256, cap_slots * 256, 64,
+                    128, 1);
+      if (st == NOMAS_OK)
+        st = encode3d(&tm.vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->v, 128, pl.nc, bh_rows, 256, cap_slots * 256,
+                      64, 128, 1);
+    }
+  }
+  if (st != NOMAS_OK) return st;
+  AttnParams p;
+  p.nq = pl.nq;
+  p.nc = pl.nc;
+  p.heads = cache->heads;
+  p.n_cache_tiles = pl.n_cache_tiles;
+  p.n_cur_tiles = pl.n_cur_tiles;
+  p.num_splits = pl.splits;
+  p.block_head_base = block * cache->heads;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.ws_o = pl.splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.ws_lse = pl.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_o_bytes) : nullptr;
+  p.k_scale = cache->k_scale;
+  p.v_scale = cache->v_scale;
+  p.scale_stride = static_cast<long long>(cap_slots);
+  p.err = err;
+  st = from_cuda(launch_segment_attn(int8, tm, p, pl.n_pairs, stream));
+  if (st == NOMAS_OK && pl.splits > 1) st = from_cuda(launch_attn_combine(p, stream));
+  return st;
+}
+
+NOMAS_API nomas_status nomas_device_error(nomas_status* status, int clear) {
+  if (status == nullptr) return NOMAS_ERR_INVALID_ARG;
+  uint32_t* err = nullptr;
+  nomas_status st = device_state(&err, nullptr);
+  if (st != NOMAS_OK) return st;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return NOMAS_ERR_CUDA;
+  if (clear && v != 0) {
+    const uint32_t z = 0;
+    if (cudaMemcpy(err, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return NOMAS_ERR_CUDA;
+  }
+  *status = static_cast<nomas_status>(v);
+  return NOMAS_OK;
+}

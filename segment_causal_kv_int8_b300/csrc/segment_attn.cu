@@ -1,0 +1,540 @@
+// segment_attn.cu - segment-causal attention over [resident KV cache ; current
+// segment] for one transformer block, on B300 tensor cores (tcgen05 + TMEM +
+// TMA), with the INT8 cache dequantised to BF16 in shared memory.
+//
+// What it computes (the "segment-wise causal joint attention" of the
+// madebyagents.com model page over the lifelong KV cache of the orcarouter.ai
+// explainer, section "Die Schleife"): per head, O = softmax(s Q K^T) V where
+// the queries are the current segment's video + text tokens and the keys are
+// the resident cache slots followed by the current segment's own tokens.
+//
+// Design (one CTA = one head x 256 query rows x one key-range split):
+//   warps 0-3   softmax for query tile 0 (rows   0..127), one thread per row
+//   warps 4-7   softmax for query tile 1 (rows 128..255)
+//   warp  8     TMA producer: Q once, then K/V tiles of 128 keys into a ring
+//   warp  9     TMEM allocator + single-thread tcgen05.mma issuer
+//   warps 12-15 (INT8 cache) dequantise staged int8 K/V tiles into the ring
+// Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 f32 columns each; the
+// bf16 probabilities P_t overwrite the first 64 columns of S_t and feed the
+// P.V product straight from tensor memory.  Softmax is online in the log2
+// domain with a lazy rescale of O (only when the running max grows by more
+// than 8, i.e. a factor 256), which is exact up to rounding.  Splits of the
+// key range write f32 partial outputs and log-sum-exps that a second kernel
+// combines in a fixed order, so results are reproducible bit for bit.
+//
+// Every wait on an mbarrier is bounded (about one second); on timeout the CTA
+// records an error, waits briefly for its own copies and MMAs, frees tensor
+// memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace nomas {
+namespace attn {
+
+constexpr int kThreads = 512;
+constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 tile: [2 panels][128 rows][128 B]
+constexpr int kPanelBytes = 128 * 128;      // 64 bf16 columns x 128 rows, 128B-swizzled
+constexpr int kI8TileBytes = 128 * 128;     // one int8 tile: [128 rows][128 B], 128B-swizzled
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // S = Q K^T (both K-major)
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, true);   // O += P V (V is N-major)
+constexpr float kLazyRescale = 8.0f;        // log2 of the tolerated growth of exp terms
+constexpr float kLn2 = 0.69314718055994531f;
+
+template <bool kInt8>
+struct Layout {
+  static constexpr int NS = kInt8 ? 3 : 5;  // bf16 ring slots (K and V tiles alternate)
+  static constexpr int NI = kInt8 ? 3 : 0;  // int8 staging slots
+  static constexpr int kQ = 0;
+  static constexpr int kRing = 2 * kTileBytes;
+  static constexpr int kStage = kRing + NS * kTileBytes;
+  static constexpr int kBars = kStage + NI * kI8TileBytes;
+  // barrier indices
+  static constexpr int bQ = 0;
+  static constexpr int bRingFull = 1;
+  static constexpr int bRingEmpty = bRingFull + NS;
+  static constexpr int bStageFull = bRingEmpty + NS;
+  static constexpr int bStageEmpty = bStageFull + NI;
+  static constexpr int bSFull = bStageEmpty + NI;  // [2]
+  static constexpr int bPFull = bSFull + 2;         // [2]
+  static constexpr int bPVDone = bPFull + 2;        // [2]
+  static constexpr int bFinal = bPVDone + 2;
+  static constexpr int kNumBars = bFinal + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for aligning the base to 1024 B
+};
+static_assert(Layout<false>::kAlloc <= 232448, "bf16 layout exceeds shared memory");
+static_assert(Layout<true>::kAlloc <= 232448, "int8 layout exceeds shared memory");
+
+struct TileInfo {
+  bool cache;
+  int row0;
+  int valid;
+};
+
+__device__ __forceinline__ TileInfo tile_info(int j, const AttnParams& p) {
+  TileInfo t;
+  if (j < p.n_cache_tiles) {
+    t.cache = true;
+    t.row0 = j * 128;
+    t.valid = min(128, p.nc - t.row0);
+  } else {
+    t.cache = false;
+    t.row0 = (j - p.n_cache_tiles) * 128;
+    t.valid = min(128, p.nq - t.row0);
+  }
+  return t;
+}
+
+// int8 code byte -> float via the 2^23 magic number: (2^23 + (c + 128)) - (2^23 + 128) = c.
+__device__ __forceinline__ float i8_to_f32(uint32_t biased, uint32_t sel) {
+  return __uint_as_float(__byte_perm(biased, 0x4B000000u, sel)) - 8388736.0f;
+}
+
+template <bool kInt8>
+__global__ void __launch_bounds__(kThreads, 1)
+    segment_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcur,
+                        const __grid_constant__ CUtensorMap tm_vcur, const __grid_constant__ CUtensorMap tm_kc,
+                        const __grid_constant__ CUtensorMap tm_vc, const AttnParams p) {
+  using L = Layout<kInt8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  AbortState* ab = reinterpret_cast<AbortState*>(smem + L::kMisc + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int head = blockIdx.y;
+  const int split = blockIdx.z;
+  const int q_row0 = blockIdx.x * 256;
+  const int n_tiles = p.n_cache_tiles + p.n_cur_tiles;
+  const int t_begin = static_cast<int>((static_cast<long long>(split) * n_tiles) / p.num_splits);
+  const int t_end = static_cast<int>((static_cast<long long>(split + 1) * n_tiles) / p.num_splits);
+  const int n_iter = t_end - t_begin;
+  const int bh = p.block_head_base + head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[L::bQ], 1);
+    for (int s = 0; s < L::NS; ++s) {
+      mbar_init(&bars[L::bRingFull + s], kInt8 ? 4 : 1);
+      mbar_init(&bars[L::bRingEmpty + s], 1);
+    }
+    for (int s = 0; s < L::NI; ++s) {
+      mbar_init(&bars[L::bStageFull + s], 1);
+      mbar_init(&bars[L::bStageEmpty + s], 4);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[L::bSFull + t], 1);
+      mbar_init(&bars[L::bPFull + t], 128);
+      mbar_init(&bars[L::bPVDone + t], 1);
+    }
+    mbar_init(&bars[L::bFinal], 1);
+    ab->flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sRing = smem + L::kRing;
+  uint8_t* sStage = smem + L::kStage;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    int r_done = 0, ri_done = 0;  // ring / staging uses issued so far
+    bool ok = true;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kcur);
+      tma_prefetch_desc(&tm_vcur);
+      if (p.n_cache_tiles > 0) {
+        tma_prefetch_desc(&tm_kc);
+        tma_prefetch_desc(&tm_vc);
+      }
+      mbar_arrive_expect_tx(&bars[L::bQ], 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_3d(sQ + t * kTileBytes + pn * kPanelBytes, &tm_q, &bars[L::bQ], pn * 64, head,
+                      q_row0 + t * 128);
+    }
+    __syncwarp();
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const TileInfo ti = tile_info(t_begin + it, p);
+      for (int kv = 0; kv < 2 && ok; ++kv) {
+        const int r = 2 * it + kv;
+        if (kInt8 && ti.cache) {
+          const int si = ri_done % (L::NI > 0 ? L::NI : 1), ui = ri_done / (L::NI > 0 ? L::NI : 1);
+          if (ui > 0 && !warp_wait(&bars[L::bStageEmpty + si], (ui - 1) & 1, ab, p.err)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint64_t* fb = &bars[L::bStageFull + si];
+            mbar_arrive_expect_tx(fb, kI8TileBytes);
+            tma_load_3d(sStage + si * kI8TileBytes, kv ? &tm_vc : &tm_kc, fb, 0, ti.row0, bh);
+          }
+          ++ri_done;
+        } else {
+          const int s = r % L::NS, u = r / L::NS;
+          if (u > 0 && !warp_wait(&bars[L::bRingEmpty + s], (u - 1) & 1, ab, p.err)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint64_t* fb = &bars[L::bRingFull + s];
+            mbar_arrive_expect_tx(fb, kTileBytes);
+            if (kInt8) {
+              mbar_arrive(fb);
+              mbar_arrive(fb);
+              mbar_arrive(fb);
+            }
+            uint8_t* dst = sRing + s * kTileBytes;
+            for (int pn = 0; pn < 2; ++pn) {
+              if (ti.cache)
+                tma_load_3d(dst + pn * kPanelBytes, kv ? &tm_vc : &tm_kc, fb, pn * 64, ti.row0, bh);
+              else
+                tma_load_3d(dst + pn * kPanelBytes, kv ? &tm_vcur : &tm_kcur, fb, pn * 64, head, ti.row0);
+            }
+          }
+        }
+        __syncwarp();
+        r_done = r + 1;
+      }
+    }
+    if (!ok) {
+      // Abort: let our own copies land before the CTA's shared memory goes away.
+      warp_wait_teardown(&bars[L::bQ], 0, 20000000ull);
+      for (int r = r_done - 1; r >= 0 && r >= r_done - 2 * (L::NS + L::NI); --r) {
+        const TileInfo ti = tile_info(t_begin + r / 2, p);
+        if (kInt8 && ti.cache) continue;
+        warp_wait_teardown(&bars[L::bRingFull + r % L::NS], (r / L::NS) & 1, 20000000ull);
+      }
+      for (int ri = ri_done - 1; ri >= 0 && ri >= ri_done - L::NI; --ri)
+        warp_wait_teardown(&bars[L::bStageFull + ri % (L::NI > 0 ? L::NI : 1)],
+                           (ri / (L::NI > 0 ? L::NI : 1)) & 1, 20000000ull);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = warp_wait(&bars[L::bQ], 0, ab, p.err);
+    tc_fence_after();
+    const uint32_t q_base = smem_u32(sQ);
+    const uint32_t ring_base = smem_u32(sRing);
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const int rk = 2 * it, sk = rk % L::NS, uk = rk / L::NS;
+      if (!warp_wait(&bars[L::bRingFull + sk], uk & 1, ab, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t) {
+        // S_t / P_t of the previous tile must be consumed by its P.V product first.
+        if (it > 0 && !warp_wait(&bars[L::bPVDone + t], (it - 1) & 1, ab, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + t * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k >> 2) * kPanelBytes + (k & 3) * 32;
+            const uint64_t a = smem_desc_sw128(q_base + t * kTileBytes + koff, 16, 1024);
+            const uint64_t b = smem_desc_sw128(ring_base + sk * kTileBytes + koff, 16, 1024);
+            mma_ss(d, a, b, kIdescS, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[L::bSFull + t]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&bars[L::bRingEmpty + sk]);
+      __syncwarp();
+      const int rv = rk + 1, sv = rv % L::NS, uv = rv / L::NS;
+      if (!warp_wait(&bars[L::bRingFull + sv], uv & 1, ab, p.err)) {
+        ok = false;
+        break;
+      }
+      for (int t = 0; t < 2; ++t) {
+        if (!warp_wait(&bars[L::bPFull + t], it & 1, ab, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + 256 + t * 128;
+          const uint32_t a_tm = tmem + t * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t b = smem_desc_sw128(ring_base + sv * kTileBytes + k * 2048, kPanelBytes, 1024);
+            mma_ts(d, a_tm + k * 8, b, kIdescO, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars[L::bPVDone + t]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&bars[L::bRingEmpty + sv]);
+      __syncwarp();
+    }
+    // Drain: all MMAs issued by this thread complete before tensor memory is freed.
+    if (lane == 0) mma_commit(&bars[L::bFinal]);
+    __syncwarp();
+    warp_wait_teardown(&bars[L::bFinal], 0, ok ? 2000000000ull : 20000000ull);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t s_col = t * 128;
+    const uint32_t o_col = 256 + t * 128;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int valid = tile_info(t_begin + it, p).valid;
+      if (!warp_wait(&bars[L::bSFull + t], it & 1, ab, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float mx = -INFINITY;
+      uint32_t v[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (32 * c < valid) {
+          tmem_ld_x32(lane_base + s_col + 32 * c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+        }
+      }
+      const float m_tile = mx * sl2;
+      const bool need = (it > 0) && (m_tile > m + kLazyRescale);
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? fast_exp2(m - m_tile) : 1.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_x32(lane_base + o_col + 32 * c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st_x32(lane_base + o_col + 32 * c, v);
+        }
+        if (need) l *= alpha;
+      }
+      if (it == 0 || need) m = m_tile;
+      const float neg_m = -m;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+        if (32 * c < valid) {
+          tmem_ld_x32(lane_base + s_col + 32 * c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float p0 = (32 * c + 2 * i < valid) ? fast_exp2(fmaf(__uint_as_float(v[2 * i]), sl2, neg_m)) : 0.0f;
+            float p1 =
+                (32 * c + 2 * i + 1 < valid) ? fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), sl2, neg_m)) : 0.0f;
+            l += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        }
+        tmem_st_x16(lane_base + s_col + 16 * c, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[L::bPFull + t]);
+    }
+    if (ok && n_iter > 0 && warp_wait(&bars[L::bPVDone + t], (n_iter - 1) & 1, ab, p.err)) {
+      tc_fence_after();
+      const int grow = q_row0 + t * 128 + row;
+      const bool live = grow < p.nq;
+      const float inv_l = 1.0f / l;
+      const float lse_val = (m + log2f(l)) * kLn2;
+      uint32_t v[32];
+      if (p.num_splits == 1) {
+        __nv_bfloat16* dst = p.out + (static_cast<size_t>(grow) * p.heads + head) * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_x32(lane_base + o_col + 32 * c, v);
+          if (live) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * inv_l, __uint_as_float(v[8 * g + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * inv_l, __uint_as_float(v[8 * g + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * inv_l, __uint_as_float(v[8 * g + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * inv_l, __uint_as_float(v[8 * g + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(dst + 32 * c + 8 * g) = w;
+            }
+          }
+        }
+        if (live && p.lse) p.lse[static_cast<size_t>(head) * p.nq + grow] = lse_val;
+      } else {
+        float* dst = p.ws_o + ((static_cast<size_t>(split) * p.heads + head) * p.nq + grow) * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_x32(lane_base + o_col + 32 * c, v);
+          if (live) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              float4 w = make_float4(__uint_as_float(v[4 * g + 0]) * inv_l, __uint_as_float(v[4 * g + 1]) * inv_l,
+                                     __uint_as_float(v[4 * g + 2]) * inv_l, __uint_as_float(v[4 * g + 3]) * inv_l);
+              *reinterpret_cast<float4*>(dst + 32 * c + 4 * g) = w;
+            }
+          }
+        }
+        if (live) p.ws_lse[(static_cast<size_t>(split) * p.heads + head) * p.nq + grow] = lse_val;
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dequantise
+    if constexpr (kInt8) {
+    const int drow = threadIdx.x - 384;  // 0..127: one tile row per thread
+    const int sw = drow & 7;
+    int ri = 0;
+    bool ok = true;
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const TileInfo ti = tile_info(t_begin + it, p);
+      if (!ti.cache) continue;
+      for (int kv = 0; kv < 2; ++kv) {
+        const int r = 2 * it + kv, s = r % L::NS, u = r / L::NS;
+        const int si = ri % L::NI, ui = ri / L::NI;
+        const float* sp = kv ? p.v_scale : p.k_scale;
+        const float sc = (drow < ti.valid) ? sp[static_cast<size_t>(bh) * p.scale_stride + ti.row0 + drow] : 0.0f;
+        if (!warp_wait(&bars[L::bStageFull + si], ui & 1, ab, p.err)) {
+          ok = false;
+          break;
+        }
+        if (u > 0 && !warp_wait(&bars[L::bRingEmpty + s], (u - 1) & 1, ab, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* src = sStage + si * kI8TileBytes + drow * 128;
+        uint8_t* dst = sRing + s * kTileBytes + drow * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+          const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float f0 = i8_to_f32(wd[e], 0x7540u) * sc;
+            const float f1 = i8_to_f32(wd[e], 0x7541u) * sc;
+            const float f2 = i8_to_f32(wd[e], 0x7542u) * sc;
+            const float f3 = i8_to_f32(wd[e], 0x7543u) * sc;
+            o[2 * e] = pack_bf16x2(f0, f1);
+            o[2 * e + 1] = pack_bf16x2(f2, f3);
+          }
+          // int8 columns 16c..16c+15 -> bf16 panel c/4, 16-byte chunks 2(c%4) and 2(c%4)+1
+          uint8_t* pd = dst + (c >> 2) * kPanelBytes;
+          const int c0 = (2 * (c & 3)) ^ sw, c1 = (2 * (c & 3) + 1) ^ sw;
+          *reinterpret_cast<uint4*>(pd + (c0 << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(pd + (c1 << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[L::bRingFull + s]);
+          mbar_arrive(&bars[L::bStageEmpty + si]);
+        }
+        ++ri;
+      }
+    }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Combine per-split partial outputs in split order: O = sum_s w_s O_s / sum_s w_s,
+// w_s = exp(lse_s - max lse), LSE = max + log(sum w_s).  One warp per (head, row).
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                                                      int splits, int heads, int nq, __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ lse) {
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= static_cast<long long>(heads) * nq) return;
+  const int h = static_cast<int>(gw / nq);
+  const int r = static_cast<int>(gw % nq);
+  float mx = -INFINITY;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ws_lse[(static_cast<size_t>(s) * heads + h) * nq + r]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.0f;
+  for (int s = 0; s < splits; ++s) {
+    const size_t row = (static_cast<size_t>(s) * heads + h) * nq + r;
+    const float w = expf(ws_lse[row] - mx);
+    const float4 o = *reinterpret_cast<const float4*>(ws_o + row * 128 + 4 * lane);
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+    wsum += w;
+  }
+  const float inv = 1.0f / wsum;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out + (static_cast<size_t>(r) * heads + h) * 128 + 4 * lane) = pk;
+  if (lse && lane == 0) lse[static_cast<size_t>(h) * nq + r] = mx + logf(wsum);
+}
+
+template <bool kInt8>
+static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, int n_pairs, cudaStream_t stream) {
+  using L = Layout<kInt8>;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(segment_attn_kernel<kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  dim3 grid(n_pairs, p.heads, p.num_splits);
+  segment_attn_kernel<kInt8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn
+
+cudaError_t launch_segment_attn(bool int8_cache, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
+                                cudaStream_t stream) {
+  return int8_cache ? attn::launch_impl<true>(tm, p, n_pairs, stream)
+                    : attn::launch_impl<false>(tm, p, n_pairs, stream);
+}
+
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(p.heads) * p.nq;
+  const long long blocks = (warps * 32 + 255) / 256;
+  attn::combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.ws_o, p.ws_lse, p.num_splits, p.heads,
+                                                                          p.nq, p.out, p.lse);
+  return cudaGetLastError();
+}
+
+int attn_smem_bytes(bool int8_cache) {
+  return int8_cache ? attn::Layout<true>::kAlloc : attn::Layout<false>::kAlloc;
+}
+
+}  // namespace nomas

@@ -1,0 +1,139 @@
+"""CPU-only checks of the C ABI library: it loads without a GPU, exports every
+entry point the header declares, and its host-side logic (descriptor checks,
+append planning, byte accounting) agrees with the oracle's cache model.
+No call here launches a kernel.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import segment_causal_kv_int8_b300 as nomas
+from oracle import ring_cache
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "nomas.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nomas_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_exported_and_bound():
+    names = _declared()
+    assert "nomas_segment_attn" in names and "nomas_rope3d_apply" in names
+    lib = ctypes.CDLL(nomas.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in nomas.EXPORTS, n
+
+
+def _desc(blocks=1, heads=2, gh=3, gw=4, cap=5, past=0, dtype=nomas.NOMAS_INT8, total=0, valid=0):
+    return nomas.nomas_kvcache(blocks, heads, 128, gh, gw, cap, past, dtype, 256, 512, 1024, 2048, total, valid, 0)
+
+
+def test_descriptor_validation():
+    ok = _desc()
+    assert nomas.nomas_kvcache_validate(ctypes.byref(ok)) == nomas.NOMAS_OK
+    cases = [
+        (dict(past=3, cap=5), nomas.NOMAS_ERR_INVALID_ARG),       # window != capacity
+        (dict(dtype=7), nomas.NOMAS_ERR_INVALID_ARG),
+        (dict(heads=0), nomas.NOMAS_ERR_INVALID_ARG),
+        (dict(total=3, valid=2), nomas.NOMAS_ERR_INVALID_ARG),    # inconsistent metadata
+    ]
+    for kw, want in cases:
+        d = _desc(**kw)
+        assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == want, kw
+    d = _desc()
+    d.head_dim = 64
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_ERR_UNSUPPORTED
+    d = _desc()
+    d.k = 257  # misaligned
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_ERR_INVALID_ARG
+    d = _desc()
+    d.k_scale = None
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_ERR_INVALID_ARG
+    d = _desc(dtype=nomas.NOMAS_BF16)
+    d.k_scale = d.v_scale = None
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_OK
+
+
+def _plan(d, n):
+    f, s, t, v = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+    st = nomas.nomas_kvcache_plan_append(ctypes.byref(d), n, f, s, t, v)
+    return st, f.value, s.value, t.value, v.value
+
+
+@pytest.mark.parametrize("window", [0, 1, 4, 18])
+def test_plan_append_matches_oracle_ring(window):
+    rng = np.random.default_rng(window)
+    cap = window if window else 40
+    d = _desc(cap=cap, past=window)
+    o = ring_cache.RingCache(1, 2, 128, 3, 4, cap, window, "int8", store=False)
+    for _ in range(50):
+        n = int(rng.integers(0, 3 * cap // 2 + 2))
+        st, first, slot, total, valid = _plan(d, n)
+        try:
+            plan = o.plan_append(n)
+        except ring_cache.CapacityError:
+            assert st == nomas.NOMAS_ERR_CAPACITY
+            continue
+        assert st == nomas.NOMAS_OK
+        if plan:
+            assert first == plan[0][0] and slot == plan[0][2]
+        else:
+            assert first == n
+        o.append(n_frames=n)
+        assert (total, valid) == (o.total_frames, o.valid_frames)
+        d.total_frames, d.valid_frames = total, valid
+
+
+def test_kvcache_bytes_matches_oracle_and_archive_arithmetic():
+    for dtype, code in (("int8", nomas.NOMAS_INT8), ("bf16", nomas.NOMAS_BF16)):
+        d = _desc(blocks=54, heads=16, gh=23, gw=40, cap=30, dtype=code)
+        o = ring_cache.RingCache(54, 16, 128, 23, 40, 30, 0, dtype, store=False)
+        assert nomas.nomas_kvcache_bytes(ctypes.byref(d)) == o.bytes()
+    d = _desc(blocks=54, heads=16, gh=23, gw=40, cap=30)
+    # within 0.5% of the 5.881 GiB per 30-frame segment the page logs
+    assert abs(nomas.nomas_kvcache_bytes(ctypes.byref(d)) / 2 ** 30 / 5.881 - 1) < 0.005
+
+
+def test_invalid_calls_return_status_without_launching():
+    d = _desc()
+    # null q
+    assert nomas.nomas_rope3d_apply(None, None, nomas.NOMAS_BF16, 12, 2, 128, 256, 1, 3, 4, 0, 1e4, 32, 48, 48,
+                                    None) == nomas.NOMAS_ERR_INVALID_ARG
+    # n_video inconsistent with frames*grid
+    assert nomas.nomas_rope3d_apply(256, None, nomas.NOMAS_BF16, 11, 2, 128, 256, 1, 3, 4, 0, 1e4, 32, 48, 48,
+                                    None) == nomas.NOMAS_ERR_INVALID_ARG
+    # odd rotary split
+    assert nomas.nomas_rope3d_apply(256, None, nomas.NOMAS_BF16, 12, 2, 128, 256, 1, 3, 4, 0, 1e4, 31, 48, 48,
+                                    None) == nomas.NOMAS_ERR_INVALID_ARG
+    # append: bad dtype, then capacity overflow (checked before any launch)
+    assert nomas.nomas_kvcache_append(ctypes.byref(d), 256, 256, 9, 1, 0, None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert nomas.nomas_kvcache_append(ctypes.byref(d), 256, 256, nomas.NOMAS_BF16, 6, 0,
+                                      None) == nomas.NOMAS_ERR_CAPACITY
+    assert d.total_frames == 0
+    # attention: block out of range, non-positive scale
+    assert nomas.nomas_segment_attn(ctypes.byref(d), 1, 256, 256, 256, 12, 0, 0.1, 256, None, None, 0, 0,
+                                    None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert nomas.nomas_segment_attn(ctypes.byref(d), 0, 256, 256, 256, 12, 0, 0.0, 256, None, None, 0, 0,
+                                    None) == nomas.NOMAS_ERR_INVALID_ARG
+    # zero-length work is a no-op that succeeds without touching the device
+    assert nomas.nomas_segment_attn(ctypes.byref(d), 0, 256, 256, 256, 0, 0, 0.1, 256, None, None, 0, 0,
+                                    None) == nomas.NOMAS_OK
+    assert nomas.nomas_kvcache_append(ctypes.byref(d), None, None, nomas.NOMAS_BF16, 0, 0, None) == nomas.NOMAS_OK
+
+
+def test_workspace_bytes_for_explicit_splits():
+    d = _desc(heads=16, gh=23, gw=40, cap=18, past=18, total=24, valid=18)
+    out = ctypes.c_size_t()
+    assert nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), 7360, 256, 1, out) == nomas.NOMAS_OK
+    assert out.value == 0
+    assert nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), 7360, 256, 4, out) == nomas.NOMAS_OK
+    nq = 7616
+    want = -(-4 * 16 * nq * 128 * 4 // 256) * 256 + -(-4 * 16 * nq * 4 // 256) * 256
+    assert out.value == want

@@ -1,0 +1,223 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Every expected value comes from the oracle on the same seeded inputs; nothing
+the GPU produces is fed back into the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import CONFIGS, current_qkv, segment_kv, small_variant
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import segment_causal_kv_int8_b300 as nomas
+    from _gpu_common import (ROPE_REL, assert_attn_close, build_caches, f64, gpu_segment, oracle_segment,
+                             to_dev)
+    from oracle import attention as o_attn
+    from oracle import int8_codec, ring_cache
+    from oracle import rope3d as o_rope
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    yield
+    torch.cuda.synchronize()
+    assert nomas.device_error(clear=True) == 0
+
+
+# ------------------------------------------------------------------ RoPE
+@pytest.mark.parametrize("name", ["c1_tiny", "c2_bf16_hist8", "c3_int8_window18", "c4_bf16_hist60"])
+def test_rope3d_matches_oracle(name):
+    wl = CONFIGS[name]
+    q, k, _ = current_qkv(wl)
+    qd, kd = to_dev(q, wl.io_dtype), to_dev(k, wl.io_dtype)
+    nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+    for dev, host in ((qd, q), (kd, k)):
+        ref = o_rope.rope3d_segment(host, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        got = f64(dev)
+        nv = wl.n_video
+        # text rows untouched, bit for bit
+        np.testing.assert_array_equal(got[nv:], host[nv:].astype(np.float64))
+        d = np.abs(got[:nv] - ref[:nv])
+        vec_inf = np.max(np.abs(ref[:nv]), axis=2, keepdims=True)
+        if wl.io_dtype == "f32":
+            assert np.max(np.max(d, axis=2, keepdims=True) / vec_inf) <= ROPE_REL
+        else:
+            # one bf16 rounding of a float32 result within 1e-5 of the exact value
+            assert np.all(d <= 2.0 ** -8 * np.abs(ref[:nv]) + ROPE_REL * vec_inf)
+
+
+def test_rope3d_large_frame_index_and_odd_split():
+    wl = small_variant(CONFIGS["c1_tiny"], io_dtype="f32", grid_h=3, grid_w=5, cur_frames=3, n_text=2)
+    q, k, _ = current_qkv(wl)
+    t0 = 1_000_003
+    for split in ((32, 48, 48), (16, 24, 24)):
+        qd = to_dev(q, "f32")
+        nomas.rope3d(qd, None, wl.cur_frames, wl.grid_h, wl.grid_w, t0, 10000.0, split)
+        ref = o_rope.rope3d_segment(q, wl.cur_frames, wl.grid_h, wl.grid_w, t0, 10000.0, split)
+        got = f64(qd)
+        vec_inf = np.max(np.abs(ref[:wl.n_video]), axis=2, keepdims=True)
+        rel = np.max(np.abs(got[:wl.n_video] - ref[:wl.n_video]), axis=2, keepdims=True) / vec_inf
+        assert rel.max() <= ROPE_REL
+
+
+# ------------------------------------------------------------------ append
+def _check_cache_bits(gc, oc):
+    if oc.dtype == "int8":
+        np.testing.assert_array_equal(gc.k.cpu().numpy(), oc.k_codes)
+        np.testing.assert_array_equal(gc.v.cpu().numpy(), oc.v_codes)
+        np.testing.assert_array_equal(gc.k_scale.cpu().numpy().view(np.uint32), oc.k_scales.view(np.uint32))
+        np.testing.assert_array_equal(gc.v_scale.cpu().numpy().view(np.uint32), oc.v_scales.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(f64(gc.k), oc.k_vals)
+        np.testing.assert_array_equal(f64(gc.v), oc.v_vals)
+    assert gc.total_frames == oc.total_frames and gc.valid_frames == oc.valid_frames
+
+
+@pytest.mark.parametrize("name", ["c1_tiny", "c2_bf16_hist8", "c3_int8_window18"])
+def test_append_bit_exact(name):
+    wl = CONFIGS[name]
+    gc, oc = build_caches(wl)
+    _check_cache_bits(gc, oc)
+
+
+@pytest.mark.parametrize("in_dtype,cache_dtype", [("f32", "int8"), ("bf16", "int8"), ("f32", "bf16"),
+                                                  ("bf16", "bf16")])
+def test_append_multi_block_window_wrap_and_long_segment(in_dtype, cache_dtype):
+    # 3 blocks, window 4 frames: segments of 3, 2, 6 (longer than the window), 1 frames.
+    blocks, heads, gh, gw, W = 3, 2, 3, 5, 4
+    wl = small_variant(CONFIGS["c1_tiny"], heads=heads, grid_h=gh, grid_w=gw, io_dtype=in_dtype,
+                       outlier_p=0.01)
+    gc = nomas.KVCache(blocks, heads, gh, gw, W, W, cache_dtype)
+    oc = ring_cache.RingCache(blocks, heads, 128, gh, gw, W, W, cache_dtype)
+    for s, f in enumerate((3, 2, 6, 1)):
+        kv = [segment_kv(wl, s, f, b) for b in range(blocks)]
+        k = np.stack([x[0] for x in kv])
+        v = np.stack([x[1] for x in kv])
+        if s == 1:
+            k[0, 3, 1] = 0.0  # an all-zero row
+            v[2, 7, 0, :5] = 0.0
+        gc.append(to_dev(k, in_dtype), to_dev(v, in_dtype))
+        oc.append(k, v)
+        _check_cache_bits(gc, oc)
+
+
+def test_append_codec_edge_rows():
+    heads, gh, gw = 1, 1, 8
+    rows = np.zeros((8, 128), np.float32)
+    rows[1, :8] = [127.0, 2.5, 3.5, -2.5, -0.5, 0.5, 126.5, -1.5]          # ties (inv = 1)
+    rows[2] = np.linspace(-1e-39, 1e-39, 128, dtype=np.float32)              # subnormal, inv overflows
+    rows[3] = np.linspace(-3e-37, 2e-37, 128, dtype=np.float32)              # tiny normal
+    rows[4] = np.float32(3e38) * np.sin(np.arange(128, dtype=np.float32))    # huge
+    rows[5, 17] = -8.0                                                       # single negative spike
+    rows[6] = np.arange(-64, 64, dtype=np.float32)
+    rows[7] = -rows[6]
+    k = rows.reshape(1, 8, 1, 128)
+    gc = nomas.KVCache(1, heads, gh, gw, 1, 0, "int8")
+    oc = ring_cache.RingCache(1, heads, 128, gh, gw, 1, 0, "int8")
+    gc.append(to_dev(k, "f32"), to_dev(k, "f32"))
+    oc.append(k, k)
+    _check_cache_bits(gc, oc)
+
+
+def test_reset_and_capacity():
+    wl = CONFIGS["c1_tiny"]
+    gc, oc = build_caches(wl)
+    k, v = segment_kv(wl, 9, 2, 0)
+    with pytest.raises(nomas.NomasError) as e:
+        gc.append(to_dev(k, "f32"), to_dev(v, "f32"))
+    assert e.value.status == nomas.NOMAS_ERR_CAPACITY
+    assert gc.total_frames == 2
+    gc.reset(zero_memory=True)
+    torch.cuda.synchronize()
+    assert gc.total_frames == 0 and gc.valid_frames == 0
+    assert int(gc.k.abs().sum()) == 0 and float(gc.k_scale.abs().sum()) == 0.0
+
+
+# ------------------------------------------------------------------ attention
+def test_attention_tiny_config_full():
+    wl = CONFIGS["c1_tiny"]
+    gc, oc = build_caches(wl)
+    q, k, v = current_qkv(wl)
+    # the attention computes in bf16: round the f32 activations once, on both sides
+    from synth import round_to_bf16
+    q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+    ref_o, ref_lse = oracle_segment(wl, oc, q, k, v)
+    for splits in (1, 2):
+        out, lse = gpu_segment(wl, gc, q, k, v, num_splits=splits)
+        assert_attn_close(out, ref_o, lse, ref_lse)
+
+
+RAGGED = [
+    # heads, grid, cached frames (hist), current frames, text, cache dtype, window
+    dict(heads=3, grid_h=5, grid_w=7, cache_frames_hist=(2, 1), cur_frames=2, n_text=9, cache_dtype="int8",
+         past_frames=0, capacity_frames=6),
+    dict(heads=2, grid_h=5, grid_w=7, cache_frames_hist=(3, 3, 3), cur_frames=3, n_text=5, cache_dtype="int8",
+         past_frames=4, capacity_frames=4),
+    dict(heads=2, grid_h=9, grid_w=15, cache_frames_hist=(2,), cur_frames=3, n_text=40, cache_dtype="bf16",
+         past_frames=0, capacity_frames=5),
+    dict(heads=1, grid_h=4, grid_w=4, cache_frames_hist=(), cur_frames=1, n_text=0, cache_dtype="bf16",
+         past_frames=0, capacity_frames=2),
+    dict(heads=2, grid_h=16, grid_w=16, cache_frames_hist=(1,), cur_frames=1, n_text=0, cache_dtype="int8",
+         past_frames=0, capacity_frames=2),
+]
+
+
+@pytest.mark.parametrize("case", range(len(RAGGED)))
+@pytest.mark.parametrize("splits", [1, 3])
+def test_attention_ragged_shapes(case, splits):
+    wl = small_variant(CONFIGS["c2_bf16_hist8"], **RAGGED[case], seed=100 + case, outlier_p=0.01)
+    gc, oc = build_caches(wl)
+    q, k, v = current_qkv(wl)
+    ref_o, ref_lse = oracle_segment(wl, oc, q, k, v)
+    out, lse = gpu_segment(wl, gc, q, k, v, num_splits=splits)
+    assert_attn_close(out, ref_o, lse, ref_lse)
+
+
+def _sample_rows(n_q, n_video, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(n_q, size=min(n_q, 80), replace=False).tolist())
+    rows |= {0, 127, 128, 255, 256, n_video - 1, n_video, n_q - 1}
+    return np.array(sorted(r for r in rows if 0 <= r < n_q))
+
+
+@pytest.mark.parametrize("name", ["c2_bf16_hist8", "c3_int8_window18", "c4_bf16_hist60"])
+def test_attention_full_size_sampled(name):
+    wl = CONFIGS[name]
+    gc, oc = build_caches(wl)
+    q, k, v = current_qkv(wl)
+    rows = _sample_rows(wl.n_q, wl.n_video, wl.seed)
+    ref_o, ref_lse = oracle_segment(wl, oc, q, k, v, rows=rows)
+    out, lse = gpu_segment(wl, gc, q, k, v, num_splits=0)
+    assert_attn_close(out, ref_o, lse, ref_lse, rows=rows)
+    out1, _ = gpu_segment(wl, gc, q, k, v, num_splits=1)
+    assert_attn_close(out1, ref_o, rows=rows)
+
+
+def test_attention_deterministic():
+    wl = CONFIGS["c3_int8_window18"]
+    gc, _ = build_caches(wl)
+    q, k, v = current_qkv(wl)
+    for splits in (1, 4):
+        a, la = gpu_segment(wl, gc, q, k, v, num_splits=splits)
+        b, lb = gpu_segment(wl, gc, q, k, v, num_splits=splits)
+        assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_invalid_arguments_launch_nothing():
+    wl = CONFIGS["c1_tiny"]
+    gc, _ = build_caches(wl)
+    q = torch.zeros((wl.n_q, wl.heads, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(nomas.NomasError) as e:
+        nomas.segment_attn(gc, 5, q, q, q, wl.n_video, wl.n_text)
+    assert e.value.status == nomas.NOMAS_ERR_INVALID_ARG
+    with pytest.raises(nomas.NomasError) as e:
+        nomas.segment_attn(gc, 0, q, q, q, wl.n_video, wl.n_text, softmax_scale=-1.0)
+    assert e.value.status == nomas.NOMAS_ERR_INVALID_ARG
+    with pytest.raises(nomas.NomasError) as e:
+        nomas.segment_attn(gc, 0, q, q, q, wl.n_video, wl.n_text, num_splits=3)   # no workspace
+    assert e.value.status == nomas.NOMAS_ERR_INVALID_ARG
