@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the segment-causal KV-cache attention hot path.
+
+One step = one pass of the whole path over one batch of synthetic input:
+reset the cache (metadata), append the history segment(s) of K/V (INT8
+quantise or BF16 copy into the ring), 3D RoPE of the current segment's Q and K,
+segment attention of the current segment over [cache ; current].  The metric is
+the attention's FLOPs (4 * Nq * Nk * 128 * heads) per step time, in TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same-shaped workload on its own
+seeded data (independent blocks; no collective on the data path) and rank 0
+prints one JSON line with the whole-job throughput (weak scaling).
+
+``--impl reference`` times the CPU oracle (the plain float64 reference the
+tests check against) on a bounded sample of the same workload, on this host's
+cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "segment-causal KV-cache attention TFLOP/s (% of B300 dense BF16 peak)"
+UNIT = "TFLOP/s"
+DEFAULT_CONFIG = "c2_bf16_hist8"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample(wl, seconds: float, block: int = 0):
+    """Time the oracle's RoPE + segment attention on a sample of query rows.
+
+    Returns (flops_per_second, description, threads).  The sample grows until
+    it takes at least ``seconds`` (capped at the whole segment).
+    """
+    import numpy as np
+
+    from oracle import attention as o_attn
+    from oracle import ring_cache as o_cache
+    from oracle import rope3d as o_rope
+    from synth import current_qkv, history_segments
+
+    oc = o_cache.RingCache(1, wl.heads, wl.head_dim, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames,
+                           wl.cache_dtype)
+    for k, v in history_segments(wl, block):
+        oc.append(k[None], v[None])
+    q, k, v = current_qkv(wl, block=block)
+    kc, vc = oc.cache_kv(0)
+    scale = o_attn.default_scale(wl.head_dim)
+    rows = 64
+    while True:
+        sel = np.linspace(0, wl.n_q - 1, rows).astype(np.int64)
+        t0 = time.perf_counter()
+        kr = o_rope.rope3d_segment(k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        qr = o_rope.rope3d_segment(q, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)[sel]
+        o_attn.segment_attention(qr, kr, v, kc, vc, scale)
+        dt = time.perf_counter() - t0
+        if dt >= seconds or rows >= wl.n_q:
+            break
+        rows = min(wl.n_q, max(rows * 2, int(rows * seconds / max(dt, 1e-3) * 1.1)))
+    flops = 4.0 * rows * wl.n_k * wl.head_dim * wl.heads
+    threads = _blas_threads()
+    desc = (f"oracle RoPE + segment attention (float64 numpy) on {rows} of {wl.n_q} query rows x all "
+            f"{wl.heads} heads x {wl.n_k} keys of {wl.name}; {dt:.1f} s")
+    return flops / dt, desc, threads, dt
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synth import CONFIGS
+
+    wl = CONFIGS[args.config]
+    per_step = max(2.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, per_step)
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, desc, threads, dt = oracle_sample(wl, per_step)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config_dict(wl, args.gpus, "oracle sample per step"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config_dict(wl, n_gpus, l2_policy):
+    return {"workload": f"{wl.name}: {wl.heads} heads x {wl.head_dim}, grid {wl.grid_h}x{wl.grid_w}, "
+                        f"{wl.cur_frames} latent frames + {wl.n_text} text queries (Nq={wl.n_q}), "
+                        f"{wl.cache_dtype} cache of {wl.n_cache} tokens (window {wl.past_frames or 'none'}), "
+                        f"Nk={wl.n_k}",
+            "heads": wl.heads, "head_dim": wl.head_dim, "n_q": wl.n_q, "n_k": wl.n_k, "n_cache": wl.n_cache,
+            "cache_dtype": wl.cache_dtype, "parallelism": f"replica x{n_gpus} (independent blocks per GPU)",
+            "l2": l2_policy}
+
+
+# ------------------------------------------------------------------ GPU arm
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import segment_causal_kv_int8_b300 as nomas
+    from synth import CONFIGS, current_qkv, history_segments
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    wl = CONFIGS[args.config]
+    block = rank  # each rank owns an independent block's data
+
+    # ---- synthetic inputs (seeded), resident in HBM before timing
+    hist = history_segments(wl, block)
+    q_h, k_h, v_h = current_qkv(wl, block=block)
+
+    def dev_t(x):
+        return torch.from_numpy(x).to(torch.bfloat16 if wl.io_dtype == "bf16" else torch.float32).to(dev)
+
+    hist_d = [(dev_t(k), dev_t(v)) for k, v in hist]
+    q0, k0, v0 = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (q_h, k_h, v_h))
+    q, k, v = q0.clone(), k0.clone(), v0.clone()
+    cache = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames, wl.cache_dtype,
+                          device=dev)
+    lse = torch.empty((wl.heads, wl.n_q), dtype=torch.float32, device=dev)
+    out = torch.empty_like(q)
+    ws_bytes, splits_used = _workspace_for(nomas, cache, wl, args.num_splits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_a0=None, ev_a1=None):
+        cache.reset(zero_memory=False)
+        for kh, vh in hist_d:
+            cache.append(kh, vh)
+        nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        if ev_a0 is not None:
+            ev_a0.record(stream)
+        nomas.segment_attn(cache, 0, q, k, v, wl.n_video, wl.n_text, out=out, lse=lse, workspace=ws,
+                           num_splits=args.num_splits)
+        if ev_a1 is not None:
+            ev_a1.record(stream)
+
+    def restage():
+        q.copy_(q0)  # RoPE works in place: fresh un-rotated inputs for every step (untimed)
+        k.copy_(k0)
+
+    for _ in range(args.warmup):
+        restage()
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    step_ms, attn_ms = [], []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.steps):
+        flush.zero_()  # evict L2 between steps (untimed)
+        restage()
+        e0, e1, a0, a1 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        e0.record(stream)
+        step(a0, a1)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        step_ms.append(e0.elapsed_time(e1))
+        attn_ms.append(a0.elapsed_time(a1))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = wl.attn_flops()
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    attn_avg = statistics.mean(attn_ms)
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world)
+
+    launches_per_step = len(hist) + 1 + 1 + (1 if splits_used > 1 else 0)
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = _load_traffic(args.config)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config_dict(wl, world, "256 MiB buffer written between timed steps (L2 flush, untimed)"),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "segment_attn_kernel" + (" + combine" if splits_used > 1 else ""),
+                         "attn_ms": attn_avg, "splits": splits_used,
+                         "peak_source": f"bf16_tflops (burst) of {src} peaks"},
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            v_cpu, desc, threads, _ = oracle_sample(wl, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": v_cpu / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                    "sample": desc}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _workspace_for(nomas, cache, wl, num_splits):
+    """Workspace bytes and split count the library uses once the history is resident."""
+    import ctypes
+    d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
+    total = sum(wl.cache_frames_hist)
+    d.total_frames = total
+    d.valid_frames = min(total, wl.window)
+    b = ctypes.c_size_t()
+    st = nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), wl.n_video, wl.n_text, num_splits,
+                                                  ctypes.byref(b))
+    if st != 0:
+        raise RuntimeError("workspace query failed")
+    if b.value == 0:
+        return 0, 1
+    return int(b.value), max(2, int(b.value // (wl.heads * wl.n_q * 128 * 4)))
+
+
+def _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world):
+    """Same step through the public API with host (pinned) inputs and a host read of the output."""
+    import torch.distributed as dist
+
+    def pin(x, bf16):
+        t = torch.from_numpy(x)
+        t = t.to(torch.bfloat16) if bf16 else t
+        return t.pin_memory()
+
+    hist_h = [(pin(k, wl.io_dtype == "bf16"), pin(v, wl.io_dtype == "bf16")) for k, v in hist]
+    qh, kh, vh = (pin(x, True) for x in (q_h, k_h, v_h))
+    out_h = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
+    hist_d = [(torch.empty_like(a, device=dev), torch.empty_like(b, device=dev)) for a, b in hist_h]
+    qd, kd, vd = (torch.empty_like(x, device=dev) for x in (qh, kh, vh))
+    cache = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames, wl.cache_dtype,
+                          device=dev)
+    ws_bytes, _ = _workspace_for(nomas, cache, wl, args.num_splits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(qd)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(a.numel() * a.element_size() * 2 for a, _ in hist_h) + 3 * qh.numel() * qh.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for (a, b), (ad, bd) in zip(hist_h, hist_d):
+            ad.copy_(a, non_blocking=True)
+            bd.copy_(b, non_blocking=True)
+        for x, xd in ((qh, qd), (kh, kd), (vh, vd)):
+            xd.copy_(x, non_blocking=True)
+        cache.reset(zero_memory=False)
+        for ad, bd in hist_d:
+            cache.append(ad, bd)
+        nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        nomas.segment_attn(cache, 0, qd, kd, vd, wl.n_video, wl.n_text, out=out, workspace=ws,
+                           num_splits=args.num_splits)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms.append(e0.elapsed_time(e1))
+    total = sum(ms)
+    if world > 1:
+        t = torch.tensor([total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    val = wl.attn_flops() * world * args.steps / (total * 1e-3) / 1e12
+    return {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": total / args.steps}
+
+
+def _load_traffic(config):
+    """DRAM bytes per attention launch from a committed ncu summary, if one matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{config}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

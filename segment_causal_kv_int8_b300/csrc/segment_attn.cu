@@ -11,9 +11,11 @@
 // Design (one CTA = one head x 256 query rows x one key-range split):
 //   warps 0-3   softmax for query tile 0 (rows   0..127), one thread per row
 //   warps 4-7   softmax for query tile 1 (rows 128..255)
-//   warp  8     TMA producer: Q once, then K/V tiles of 128 keys into a ring
+//   warp  8     TMA producer: Q once, then K/V tiles of 128 keys (into the
+//               ring for a BF16 cache, into int8 staging slots for INT8)
 //   warp  9     TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 12-15 (INT8 cache) dequantise staged int8 K/V tiles into the ring
+//   warps 12-15 (INT8 cache) fill the ring: dequantise staged int8 tiles,
+//               fetch current-segment tiles by TMA
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 f32 columns each; the
 // bf16 probabilities P_t overwrite the first 64 columns of S_t and feed the
 // P.V product straight from tensor memory.  Softmax is online in the log2
@@ -154,6 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // BF16 cache: fills every ring slot.  INT8 cache: loads int8 cache tiles
+    // into the staging slots only; the dequantising warps fill the ring (each
+    // ring has exactly one filler, so a filler never waits on an empty-barrier
+    // more than one phase ahead of it).
     int r_done = 0, ri_done = 0;  // ring / staging uses issued so far
     bool ok = true;
     if (lane == 0) {
@@ -175,8 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = tile_info(t_begin + it, p);
       for (int kv = 0; kv < 2 && ok; ++kv) {
         const int r = 2 * it + kv;
-        if (kInt8 && ti.cache) {
-          const int si = ri_done % (L::NI > 0 ? L::NI : 1), ui = ri_done / (L::NI > 0 ? L::NI : 1);
+        if constexpr (kInt8) {
+          if (!ti.cache) continue;
+          const int si = ri_done % L::NI, ui = ri_done / L::NI;
           if (ui > 0 && !warp_wait(&bars[L::bStageEmpty + si], (ui - 1) & 1, ab, p.err)) {
             ok = false;
             break;
@@ -196,11 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             uint64_t* fb = &bars[L::bRingFull + s];
             mbar_arrive_expect_tx(fb, kTileBytes);
-            if (kInt8) {
-              mbar_arrive(fb);
-              mbar_arrive(fb);
-              mbar_arrive(fb);
-            }
             uint8_t* dst = sRing + s * kTileBytes;
             for (int pn = 0; pn < 2; ++pn) {
               if (ti.cache)
@@ -209,22 +211,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst + pn * kPanelBytes, kv ? &tm_vcur : &tm_kcur, fb, pn * 64, head, ti.row0);
             }
           }
+          r_done = r + 1;
         }
         __syncwarp();
-        r_done = r + 1;
       }
     }
     if (!ok) {
       // Abort: let our own copies land before the CTA's shared memory goes away.
       warp_wait_teardown(&bars[L::bQ], 0, 20000000ull);
-      for (int r = r_done - 1; r >= 0 && r >= r_done - 2 * (L::NS + L::NI); --r) {
-        const TileInfo ti = tile_info(t_begin + r / 2, p);
-        if (kInt8 && ti.cache) continue;
+      for (int r = r_done - 1; r >= 0 && r >= r_done - L::NS; --r)
         warp_wait_teardown(&bars[L::bRingFull + r % L::NS], (r / L::NS) & 1, 20000000ull);
+      if constexpr (kInt8) {
+        for (int ri = ri_done - 1; ri >= 0 && ri >= ri_done - L::NI; --ri)
+          warp_wait_teardown(&bars[L::bStageFull + ri % L::NI], (ri / L::NI) & 1, 20000000ull);
       }
-      for (int ri = ri_done - 1; ri >= 0 && ri >= ri_done - L::NI; --ri)
-        warp_wait_teardown(&bars[L::bStageFull + ri % (L::NI > 0 ? L::NI : 1)],
-                           (ri / (L::NI > 0 ? L::NI : 1)) & 1, 20000000ull);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -403,59 +403,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 12) {
-    // ------------------------------------------------------------ dequantise
+    // ------------------------------------------------------------ ring filler (INT8 cache)
+    // Fills every ring slot in order: int8 cache tiles are dequantised from
+    // the staging slots (x_hat = bf16(code * scale)), current-segment bf16
+    // tiles are fetched by TMA (issued by warp 12).  All four warps wait for
+    // the slot to be empty and arrive once on its full-barrier (count 4).
     if constexpr (kInt8) {
-    const int drow = threadIdx.x - 384;  // 0..127: one tile row per thread
-    const int sw = drow & 7;
-    int ri = 0;
-    bool ok = true;
-    for (int it = 0; it < n_iter && ok; ++it) {
-      const TileInfo ti = tile_info(t_begin + it, p);
-      if (!ti.cache) continue;
-      for (int kv = 0; kv < 2; ++kv) {
-        const int r = 2 * it + kv, s = r % L::NS, u = r / L::NS;
-        const int si = ri % L::NI, ui = ri / L::NI;
-        const float* sp = kv ? p.v_scale : p.k_scale;
-        const float sc = (drow < ti.valid) ? sp[static_cast<size_t>(bh) * p.scale_stride + ti.row0 + drow] : 0.0f;
-        if (!warp_wait(&bars[L::bStageFull + si], ui & 1, ab, p.err)) {
-          ok = false;
-          break;
-        }
-        if (u > 0 && !warp_wait(&bars[L::bRingEmpty + s], (u - 1) & 1, ab, p.err)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* src = sStage + si * kI8TileBytes + drow * 128;
-        uint8_t* dst = sRing + s * kTileBytes + drow * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
-          const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-          uint32_t o[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float f0 = i8_to_f32(wd[e], 0x7540u) * sc;
-            const float f1 = i8_to_f32(wd[e], 0x7541u) * sc;
-            const float f2 = i8_to_f32(wd[e], 0x7542u) * sc;
-            const float f3 = i8_to_f32(wd[e], 0x7543u) * sc;
-            o[2 * e] = pack_bf16x2(f0, f1);
-            o[2 * e + 1] = pack_bf16x2(f2, f3);
+      const int drow = threadIdx.x - 384;  // 0..127: one tile row per thread
+      const int sw = drow & 7;
+      int ri = 0, r_tma = 0;
+      bool ok = true;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const TileInfo ti = tile_info(t_begin + it, p);
+        for (int kv = 0; kv < 2; ++kv) {
+          const int r = 2 * it + kv, s = r % L::NS, u = r / L::NS;
+          if (!ti.cache) {
+            if (u > 0 && !warp_wait(&bars[L::bRingEmpty + s], (u - 1) & 1, ab, p.err)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              uint64_t* fb = &bars[L::bRingFull + s];
+              if (warp == 12) {
+                mbar_arrive_expect_tx(fb, kTileBytes);
+                uint8_t* dst = sRing + s * kTileBytes;
+                for (int pn = 0; pn < 2; ++pn)
+                  tma_load_3d(dst + pn * kPanelBytes, kv ? &tm_vcur : &tm_kcur, fb, pn * 64, head, ti.row0);
+              } else {
+                mbar_arrive(fb);
+              }
+            }
+            r_tma = r + 1;
+            __syncwarp();
+            continue;
           }
-          // int8 columns 16c..16c+15 -> bf16 panel c/4, 16-byte chunks 2(c%4) and 2(c%4)+1
-          uint8_t* pd = dst + (c >> 2) * kPanelBytes;
-          const int c0 = (2 * (c & 3)) ^ sw, c1 = (2 * (c & 3) + 1) ^ sw;
-          *reinterpret_cast<uint4*>(pd + (c0 << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(pd + (c1 << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          const int si = ri % L::NI, ui = ri / L::NI;
+          const float* sp = kv ? p.v_scale : p.k_scale;
+          const float sc =
+              (drow < ti.valid) ? sp[static_cast<size_t>(bh) * p.scale_stride + ti.row0 + drow] : 0.0f;
+          if (!warp_wait(&bars[L::bStageFull + si], ui & 1, ab, p.err)) {
+            ok = false;
+            break;
+          }
+          if (u > 0 && !warp_wait(&bars[L::bRingEmpty + s], (u - 1) & 1, ab, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = sStage + si * kI8TileBytes + drow * 128;
+          uint8_t* dst = sRing + s * kTileBytes + drow * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+            const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float f0 = i8_to_f32(wd[e], 0x7540u) * sc;
+              const float f1 = i8_to_f32(wd[e], 0x7541u) * sc;
+              const float f2 = i8_to_f32(wd[e], 0x7542u) * sc;
+              const float f3 = i8_to_f32(wd[e], 0x7543u) * sc;
+              o[2 * e] = pack_bf16x2(f0, f1);
+              o[2 * e + 1] = pack_bf16x2(f2, f3);
+            }
+            // int8 columns 16c..16c+15 -> bf16 panel c/4, 16-byte chunks 2(c%4) and 2(c%4)+1
+            uint8_t* pd = dst + (c >> 2) * kPanelBytes;
+            const int c0 = (2 * (c & 3)) ^ sw, c1 = (2 * (c & 3) + 1) ^ sw;
+            *reinterpret_cast<uint4*>(pd + (c0 << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(pd + (c1 << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars[L::bRingFull + s]);
+            mbar_arrive(&bars[L::bStageEmpty + si]);
+          }
+          ++ri;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars[L::bRingFull + s]);
-          mbar_arrive(&bars[L::bStageEmpty + si]);
-        }
-        ++ri;
       }
-    }
+      if (!ok && warp == 12) {
+        // Abort: wait for the current-tile copies this warp issued.
+        for (int r = r_tma - 1; r >= 0 && r >= r_tma - L::NS; --r) {
+          const TileInfo ti = tile_info(t_begin + r / 2, p);
+          if (ti.cache) continue;
+          warp_wait_teardown(&bars[L::bRingFull + r % L::NS], (r / L::NS) & 1, 20000000ull);
+        }
+      }
     }
   }
 

@@ -170,7 +170,8 @@ RAGGED = [
 @pytest.mark.parametrize("case", range(len(RAGGED)))
 @pytest.mark.parametrize("splits", [1, 3])
 def test_attention_ragged_shapes(case, splits):
-    wl = small_variant(CONFIGS["c2_bf16_hist8"], **RAGGED[case], seed=100 + case, outlier_p=0.01)
+    # N(0,1) inputs: the domain the attention tolerance is stated for
+    wl = small_variant(CONFIGS["c2_bf16_hist8"], **RAGGED[case], seed=100 + case)
     gc, oc = build_caches(wl)
     q, k, v = current_qkv(wl)
     ref_o, ref_lse = oracle_segment(wl, oc, q, k, v)
