@@ -9,7 +9,7 @@ on any status other than ``NOMAS_OK``.
 
 There is no CPU fallback: importing this package loads the shared library and
 fails loudly when it has not been built (``python -m
-segment_causal_kv_int8_b300._build``).
+segment_causal_kv_int8_b300/_build.py``).
 """
 from __future__ import annotations
 
@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libnomas.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m segment_causal_kv_int8_b300._build` "
+        f"{LIB_PATH} is missing: build it with `python segment_causal_kv_int8_b300/_build.py` "
         "(there is no fallback implementation)")
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -85,7 +85,11 @@ EXPORTS = {
 }
 
 for _name, (_res, _args) in EXPORTS.items():
-    _fn = getattr(_lib, _name)
+    try:
+        _fn = getattr(_lib, _name)
+    except AttributeError as _e:
+        raise ImportError(f"{LIB_PATH} lacks {_name}: rebuild it with "
+                          "`python segment_causal_kv_int8_b300/_build.py`") from _e
     _fn.restype = _res
     _fn.argtypes = _args
     globals()[_name] = _fn

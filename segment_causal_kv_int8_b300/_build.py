@@ -1,6 +1,7 @@
 """Build the CUDA library ``libnomas.so`` in-tree with nvcc for sm_103a.
 
-Usage: ``python -m segment_causal_kv_int8_b300._build [--debug]``.  The library
+Usage: ``python segment_causal_kv_int8_b300/_build.py [-v]`` (run by path, so
+that building never imports the package, which loads the library).  The library
 links the CUDA runtime statically and resolves the driver's tensor-map encoder
 at run time, so loading it needs no GPU driver.
 """
