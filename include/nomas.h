@@ -193,6 +193,34 @@ nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const
                                 cudaStream_t stream);
 
 /*
+ * Scratch capacity, in bytes, of nomas_segment_attn_noalloc (one array per
+ * device, held for the life of the process).
+ */
+#define NOMAS_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * nomas_segment_attn without a workspace argument: the split-KV scratch lives
+ * in a static device array of NOMAS_NOALLOC_SCRATCH_BYTES inside the library,
+ * and the call allocates nothing.  The pages have no counterpart; it exists
+ * for callers that cannot allocate device memory on this path (an engine that
+ * has reserved nearly all of HBM for its own pools, or a latency-bound loop
+ * that cannot accept an allocation's implicit synchronisation).
+ *
+ * Arguments as nomas_segment_attn.  Returns NOMAS_ERR_CAPACITY, launching
+ * nothing, when the split count asked for (or chosen automatically for
+ * num_splits = 0) needs more scratch than NOMAS_NOALLOC_SCRATCH_BYTES;
+ * nomas_segment_attn_workspace_bytes gives the need.  Every call shares the
+ * array and it keeps the last call's contents (nothing in it must start at
+ * zero); calls whose kernels overlap on the GPU race on it.  The first call on
+ * a device looks up the array's address with that device current, so make it
+ * before any stream capture.
+ */
+nomas_status nomas_segment_attn_noalloc(const nomas_kvcache* cache, int32_t block, const void* q,
+                                        const void* k_cur, const void* v_cur, int32_t n_video,
+                                        int32_t n_text, float softmax_scale, void* out, float* lse,
+                                        int32_t num_splits, cudaStream_t stream);
+
+/*
  * Start a new session (the resident service's new session_id, "Setup" and the
  * JSON turns on the inferencekey.com RTX 4090 test page): total_frames and
  * valid_frames to 0; with zero_memory != 0 also enqueue a kernel that clears

@@ -423,3 +423,63 @@ NOMAS_API nomas_status nomas_device_error(nomas_status* status, int clear) {
   *status = static_cast<nomas_status>(v);
   return NOMAS_OK;
 }
+
+// ---------------------------------------------------------------------------
+// nomas_segment_attn_noalloc: the same attention, with its split-KV scratch
+// in a fixed device array instead of a caller-provided workspace.
+//
+// Some callers cannot allocate device memory on this path: a serving engine
+// that reserves nearly all of HBM for its own pools at start-up (a cudaMalloc
+// here would fail or fragment that reservation), or a latency-bound loop where
+// an allocation's implicit device synchronisation is not acceptable.  They call
+// this entry point and pass only inputs and outputs.
+//
+// The scratch is one array per device, kNoAllocScratchBytes long, held by every
+// device that loads this library for as long as the process lives.  All calls
+// share it and it keeps whatever the last call left there; nothing in it needs
+// to start at zero (every split writes each partial row before the combine
+// reads it).  Two calls whose kernels overlap on the GPU (different streams,
+// or different host threads without ordering) race on it.  The first call on
+// a device looks up the array's device address (cudaGetSymbolAddress) with
+// that device current; make that first call before any stream capture.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOMAS_NOALLOC_SCRATCH_BYTES];
+
+namespace nomas {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once per device.
+nomas_status noalloc_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NOMAS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return NOMAS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return NOMAS_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return NOMAS_OK;
+}
+}  // namespace
+}  // namespace nomas
+
+NOMAS_API nomas_status nomas_segment_attn_noalloc(const nomas_kvcache* cache, int32_t block, const void* q,
+                                                  const void* k_cur, const void* v_cur, int32_t n_video,
+                                                  int32_t n_text, float softmax_scale, void* out, float* lse,
+                                                  int32_t num_splits, cudaStream_t stream) {
+  size_t need = 0;
+  nomas_status st = nomas_segment_attn_workspace_bytes(cache, n_video, n_text, num_splits, &need);
+  if (st != NOMAS_OK) return st;
+  if (need > static_cast<size_t>(NOMAS_NOALLOC_SCRATCH_BYTES)) return NOMAS_ERR_CAPACITY;
+  void* scratch = nullptr;
+  if (need > 0) {
+    st = noalloc_scratch(&scratch);
+    if (st != NOMAS_OK) return st;
+  }
+  return nomas_segment_attn(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, scratch,
+                            need, num_splits, stream);
+}
