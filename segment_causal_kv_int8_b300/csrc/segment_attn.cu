@@ -47,6 +47,12 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // S = Q K^T (bot
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, true);   // O += P V (V is N-major)
 constexpr float kLazyRescale = 8.0f;        // log2 of the tolerated growth of exp terms
 constexpr float kLn2 = 0.69314718055994531f;
+// Register budget per warpgroup after the role split (launch: 128 per thread x
+// 512 threads).  The softmax warpgroups hold a whole 128-column score row;
+// 2 x 128 x 184 + 128 x 64 + 128 x 80 = 65536, the CTA's launch allocation.
+constexpr uint32_t kSoftmaxRegs = 184;
+constexpr uint32_t kControlRegs = 64;   // warps 8-11: TMA producer, MMA issuer
+constexpr uint32_t kFillerRegs = 80;    // warps 12-15: INT8 ring fillers
 
 template <bool kInt8>
 struct Layout {
@@ -153,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sRing = smem + L::kRing;
   uint8_t* sStage = smem + L::kStage;
+
+  if (warp >= 8 && warp < 12) regs_shrink<kControlRegs>();
+  if (warp >= 12) regs_shrink<kFillerRegs>();
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -295,6 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     warp_wait_teardown(&bars[L::bFinal], 0, ok ? 2000000000ull : 20000000ull);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    // One thread per query row.  Per key tile: the whole 128-column score row
+    // comes out of tensor memory in one batch, the row maximum is a tree of
+    // three-input maxima, and the exponentials use packed f32x2 FMAs with four
+    // independent packed accumulators for the row sum.  The running maximum m
+    // (log2 domain) only moves when the tile maximum exceeds it by more than
+    // kLazyRescale; O and l are then rescaled by exp2(m_old - m_new).
+    regs_grow<kSoftmaxRegs>();
     const int t = warp >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -302,7 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_col = t * 128;
     const uint32_t o_col = 256 + t * 128;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.0f;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    float m = -INFINITY;
+    uint64_t lacc[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial row sums (0.0f bits are 0)
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int valid = tile_info(t_begin + it, p).valid;
@@ -311,54 +329,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float mx = -INFINITY;
-      uint32_t v[32];
+      uint32_t v[128];
+      tmem_ld_x64_nowait(lane_base + s_col, v);
+      tmem_ld_x64_nowait(lane_base + s_col + 64, v + 64);
+      tmem_wait_ld();
+      if (valid < 128) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (32 * c < valid) {
-          tmem_ld_x32(lane_base + s_col + 32 * c, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * c + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
-        }
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) v[i] = __float_as_uint(-INFINITY);
       }
-      const float m_tile = mx * sl2;
-      const bool need = (it > 0) && (m_tile > m + kLazyRescale);
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? fast_exp2(m - m_tile) : 1.0f;
+      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; i += 8) {
+        m0 = fmax3(m0, __uint_as_float(v[i + 0]), __uint_as_float(v[i + 1]));
+        m1 = fmax3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        m2 = fmax3(m2, __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+        m3 = fmax3(m3, __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+      }
+      const float m_tile = fmax3(m0, m1, fmaxf(m2, m3)) * sl2;
+      const bool need = m_tile > m + kLazyRescale;  // always true on the first tile (m = -inf)
+      const bool any_need = __any_sync(0xffffffffu, need);
+      float alpha = 1.0f;
+      if (any_need) {
+        const float m_new = need ? m_tile : m;
+        alpha = fast_exp2(m - m_new);  // 0 on the first tile, 1 where nothing moves
+        const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lacc[k] = f2_mul(lacc[k], a2);
+        m = m_new;
+      }
+      const uint64_t negm = f2_pack(-m, -m);
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const uint64_t x = f2_fma(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2x2, negm);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        lacc[i & 3] = f2_add(lacc[i & 3], f2_pack(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      tmem_st_x64(lane_base + s_col, pk);
+      if (any_need && it > 0) {
+        // O_t holds the previous tiles' P.V (complete: S_t of this tile was
+        // issued after it); bring it to the new reference maximum.
+        const uint64_t a2 = f2_pack(alpha, alpha);
+        uint32_t o[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          tmem_ld_x32(lane_base + o_col + 32 * c, v);
+          tmem_ld_x32(lane_base + o_col + 32 * c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st_x32(lane_base + o_col + 32 * c, v);
-        }
-        if (need) l *= alpha;
-      }
-      if (it == 0 || need) m = m_tile;
-      const float neg_m = -m;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-        if (32 * c < valid) {
-          tmem_ld_x32(lane_base + s_col + 32 * c, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float p0 = (32 * c + 2 * i < valid) ? fast_exp2(fmaf(__uint_as_float(v[2 * i]), sl2, neg_m)) : 0.0f;
-            float p1 =
-                (32 * c + 2 * i + 1 < valid) ? fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), sl2, neg_m)) : 0.0f;
-            l += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 32; i += 2) {
+            const uint64_t x = f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            o[i] = __float_as_uint(x0);
+            o[i + 1] = __float_as_uint(x1);
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+          tmem_st_x32(lane_base + o_col + 32 * c, o);
         }
-        tmem_st_x16(lane_base + s_col + 16 * c, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[L::bPFull + t]);
+    }
+    float l;
+    {
+      const uint64_t s01 = f2_add(lacc[0], lacc[1]), s23 = f2_add(lacc[2], lacc[3]);
+      float a, b;
+      f2_unpack(f2_add(s01, s23), a, b);
+      l = a + b;
     }
     if (ok && n_iter > 0 && warp_wait(&bars[L::bPVDone + t], (n_iter - 1) & 1, ab, p.err)) {
       tc_fence_after();
