@@ -49,10 +49,10 @@ constexpr float kLazyRescale = 8.0f;        // log2 of the tolerated growth of e
 constexpr float kLn2 = 0.69314718055994531f;
 // Register budget per warpgroup after the role split (launch: 128 per thread x
 // 512 threads).  The softmax warpgroups hold a whole 128-column score row;
-// 2 x 128 x 184 + 128 x 64 + 128 x 80 = 65536, the CTA's launch allocation.
+// 2 x 128 x 184 + 2 x 128 x 72 = 65536, the CTA's launch allocation.
 constexpr uint32_t kSoftmaxRegs = 184;
-constexpr uint32_t kControlRegs = 64;   // warps 8-11: TMA producer, MMA issuer
-constexpr uint32_t kFillerRegs = 80;    // warps 12-15: INT8 ring fillers
+constexpr uint32_t kControlRegs = 72;   // warps 8-11: TMA producer, MMA issuer
+constexpr uint32_t kFillerRegs = 72;    // warps 12-15: INT8 ring fillers
 
 template <bool kInt8>
 struct Layout {
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[L::bSFull + t], 1);
-      mbar_init(&bars[L::bPFull + t], 128);
+      mbar_init(&bars[L::bPFull + t], 4);  // one arrival per softmax warp
       mbar_init(&bars[L::bPVDone + t], 1);
     }
     mbar_init(&bars[L::bFinal], 1);
@@ -237,71 +237,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    bool ok = warp_wait(&bars[L::bQ], 0, ab, p.err);
-    tc_fence_after();
-    const uint32_t q_base = smem_u32(sQ);
-    const uint32_t ring_base = smem_u32(sRing);
-    for (int it = 0; it < n_iter && ok; ++it) {
-      const int rk = 2 * it, sk = rk % L::NS, uk = rk / L::NS;
-      if (!warp_wait(&bars[L::bRingFull + sk], uk & 1, ab, p.err)) {
-        ok = false;
-        break;
-      }
+    // One lane issues every tcgen05.mma.  Order on the tensor pipe:
+    //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+    // so the softmax of tile t for key tile j overlaps PV of the other query
+    // tile and S of the next key tile (1024 MMA cycles).  S_t(j+1) overwrites
+    // the columns P_t(j) lives in without waiting for PV_t(j): tcgen05.mma
+    // operations issued by one thread execute in issue order, so PV_t(j) has
+    // read P_t(j) before S_t(j+1) writes there.  A commit after S_t(j+1)
+    // therefore also covers PV_t(j), which is what lets the softmax rescale
+    // O_t once it sees S_t(j+1).
+    bool ok = true;
+    if (lane == 0) {
+      ok = lane_wait(&bars[L::bQ], 0, ab, p.err);
       tc_fence_after();
-      for (int t = 0; t < 2; ++t) {
-        // S_t / P_t of the previous tile must be consumed by its P.V product first.
-        if (it > 0 && !warp_wait(&bars[L::bPVDone + t], (it - 1) & 1, ab, p.err)) {
+      const uint32_t q_base = smem_u32(sQ);
+      const uint32_t ring_base = smem_u32(sRing);
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t d = tmem + t * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (k >> 2) * kPanelBytes + (k & 3) * 32;
+          const uint64_t a = smem_desc_sw128(q_base + t * kTileBytes + koff, 16, 1024);
+          const uint64_t b = smem_desc_sw128(ring_base + slot * kTileBytes + koff, 16, 1024);
+          mma_ss(d, a, b, kIdescS, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[L::bSFull + t]);
+      };
+      auto issue_pv = [&](int t, int slot, bool accumulate) {
+        const uint32_t d = tmem + 256 + t * 128;
+        const uint32_t a_tm = tmem + t * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t b = smem_desc_sw128(ring_base + slot * kTileBytes + k * 2048, kPanelBytes, 1024);
+          mma_ts(d, a_tm + k * 8, b, kIdescO, (accumulate || k > 0) ? 1u : 0u);
+        }
+      };
+      // K of key tile j sits in ring use 2j, V in ring use 2j + 1.
+      if (ok && n_iter > 0) {
+        ok = lane_wait(&bars[L::bRingFull + 0], 0, ab, p.err);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          issue_s(1, 0);
+          mma_commit(&bars[L::bRingEmpty + 0]);
+        }
+      }
+      for (int j = 0; j < n_iter && ok; ++j) {
+        const bool last = (j + 1 == n_iter);
+        const int rv = 2 * j + 1, sv = rv % L::NS;
+        const int rk = 2 * j + 2, sk = rk % L::NS;
+        if (!lane_wait(&bars[L::bRingFull + sv], (rv / L::NS) & 1, ab, p.err) ||
+            !lane_wait(&bars[L::bPFull + 0], j & 1, ab, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t d = tmem + t * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t koff = (k >> 2) * kPanelBytes + (k & 3) * 32;
-            const uint64_t a = smem_desc_sw128(q_base + t * kTileBytes + koff, 16, 1024);
-            const uint64_t b = smem_desc_sw128(ring_base + sk * kTileBytes + koff, 16, 1024);
-            mma_ss(d, a, b, kIdescS, k > 0 ? 1u : 0u);
+        issue_pv(0, sv, j > 0);
+        if (last) mma_commit(&bars[L::bPVDone + 0]);
+        if (!last) {
+          if (!lane_wait(&bars[L::bRingFull + sk], (rk / L::NS) & 1, ab, p.err)) {
+            ok = false;
+            break;
           }
-          mma_commit(&bars[L::bSFull + t]);
+          tc_fence_after();
+          issue_s(0, sk);
         }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&bars[L::bRingEmpty + sk]);
-      __syncwarp();
-      const int rv = rk + 1, sv = rv % L::NS, uv = rv / L::NS;
-      if (!warp_wait(&bars[L::bRingFull + sv], uv & 1, ab, p.err)) {
-        ok = false;
-        break;
-      }
-      for (int t = 0; t < 2; ++t) {
-        if (!warp_wait(&bars[L::bPFull + t], it & 1, ab, p.err)) {
+        if (!lane_wait(&bars[L::bPFull + 1], j & 1, ab, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t d = tmem + 256 + t * 128;
-          const uint32_t a_tm = tmem + t * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t b = smem_desc_sw128(ring_base + sv * kTileBytes + k * 2048, kPanelBytes, 1024);
-            mma_ts(d, a_tm + k * 8, b, kIdescO, (it > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars[L::bPVDone + t]);
+        issue_pv(1, sv, j > 0);
+        mma_commit(&bars[L::bRingEmpty + sv]);
+        if (last) {
+          mma_commit(&bars[L::bPVDone + 1]);
+        } else {
+          issue_s(1, sk);
+          mma_commit(&bars[L::bRingEmpty + sk]);
         }
-        __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&bars[L::bRingEmpty + sv]);
-      __syncwarp();
+      // Drain: all MMAs issued by this thread complete before tensor memory is freed.
+      mma_commit(&bars[L::bFinal]);
+      lane_wait_teardown(&bars[L::bFinal], 0, ok ? 2000000000ull : 20000000ull);
     }
-    // Drain: all MMAs issued by this thread complete before tensor memory is freed.
-    if (lane == 0) mma_commit(&bars[L::bFinal]);
     __syncwarp();
-    warp_wait_teardown(&bars[L::bFinal], 0, ok ? 2000000000ull : 20000000ull);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     // One thread per query row.  Per key tile: the whole 128-column score row
@@ -391,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars[L::bPFull + t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[L::bPFull + t]);
     }
     float l;
     {
@@ -400,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2_unpack(f2_add(s01, s23), a, b);
       l = a + b;
     }
-    if (ok && n_iter > 0 && warp_wait(&bars[L::bPVDone + t], (n_iter - 1) & 1, ab, p.err)) {
+    if (ok && n_iter > 0 && warp_wait(&bars[L::bPVDone + t], 0, ab, p.err)) {
       tc_fence_after();
       const int grow = q_row0 + t * 128 + row;
       const bool live = grow < p.nq;

@@ -92,6 +92,35 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortS
   }
 }
 
+// Single-thread bounded wait (for roles that run on one elected lane).  Same
+// contract as warp_wait.
+__device__ __forceinline__ bool lane_wait(uint64_t* bar, uint32_t parity, AbortState* ab, uint32_t* err_word) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 63) == 0) {
+      if (ab->flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        ab->flag = 1;
+        if (err_word) atomicCAS(err_word, 0u, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Single-thread teardown wait: at most limit_ns, never raises the abort flag.
+__device__ __forceinline__ bool lane_wait_teardown(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t addr = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 63) == 63 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Bounded wait used only while tearing down after an abort: waits at most
 // `limit_ns` and never raises the abort flag.
 __device__ __forceinline__ bool warp_wait_teardown(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
