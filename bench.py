@@ -238,6 +238,13 @@ def run_ours(args):
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
 
+    def evict_l2():
+        # Write a buffer twice the L2 size, then read it back: the inputs leave
+        # L2 and the flush's own dirty lines are written back here, outside the
+        # timed step, instead of during it.
+        flush.zero_()
+        flush.view(torch.int32).sum()
+
     def step(ev_a0=None, ev_a1=None):
         cache.reset(zero_memory=False)
         for kh, vh in hist_d:
@@ -271,7 +278,7 @@ def run_ours(args):
     # events.  Each step is bracketed by its own events; the L2 flush and the
     # restaging copy sit between steps, outside them.
     for i in range(args.steps):
-        flush.zero_()  # evict L2 between steps (untimed)
+        evict_l2()  # untimed, between steps
         restage()
         e0, e1, a0, a1 = evs[i]
         e0.record(stream)
@@ -308,7 +315,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _config_dict(wl, world, "256 MiB buffer written between timed steps (L2 flush, untimed)"),
+            "config": _config_dict(wl, world, "256 MiB buffer written then read between timed steps (L2 flush, untimed)"),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "segment_attn_kernel" + (" + combine" if splits_used > 1 else ""),

@@ -237,7 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // One lane issues every tcgen05.mma.  Order on the tensor pipe:
+    // The whole warp runs this loop (operands stay warp-uniform) and an
+    // elected lane issues each tcgen05.mma and commit.  Order on the tensor
+    // pipe:
     //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
     // so the softmax of tile t for key tile j overlaps PV of the other query
     // tile and S of the next key tile (1024 MMA cycles).  S_t(j+1) overwrites
@@ -246,81 +248,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     // read P_t(j) before S_t(j+1) writes there.  A commit after S_t(j+1)
     // therefore also covers PV_t(j), which is what lets the softmax rescale
     // O_t once it sees S_t(j+1).
-    bool ok = true;
-    if (lane == 0) {
-      ok = lane_wait(&bars[L::bQ], 0, ab, p.err);
-      tc_fence_after();
-      const uint32_t q_base = smem_u32(sQ);
-      const uint32_t ring_base = smem_u32(sRing);
-      auto issue_s = [&](int t, int slot) {
-        const uint32_t d = tmem + t * 128;
+    bool ok = warp_wait(&bars[L::bQ], 0, ab, p.err);
+    tc_fence_after();
+    // Descriptors of offset 0; adding (byte offset >> 4) advances the start
+    // address field (shared addresses stay below 256 KB, so it never carries).
+    const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t k_desc = smem_desc_sw128(smem_u32(sRing), 16, 1024);           // K-major (K tiles)
+    const uint64_t v_desc = smem_desc_sw128(smem_u32(sRing), kPanelBytes, 1024);  // N-major (V tiles)
+    auto commit = [=](int bar) {
+      if (elect_one()) mma_commit(&bars[bar]);
+      __syncwarp();
+    };
+    auto issue_s = [=](int t, int slot) {
+      const uint32_t d = tmem + t * 128;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (k >> 2) * kPanelBytes + (k & 3) * 32;
-          const uint64_t a = smem_desc_sw128(q_base + t * kTileBytes + koff, 16, 1024);
-          const uint64_t b = smem_desc_sw128(ring_base + slot * kTileBytes + koff, 16, 1024);
+          const uint64_t a = q_desc + ((t * kTileBytes + koff) >> 4);
+          const uint64_t b = k_desc + ((slot * kTileBytes + koff) >> 4);
           mma_ss(d, a, b, kIdescS, k > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[L::bSFull + t]);
-      };
-      auto issue_pv = [&](int t, int slot, bool accumulate) {
-        const uint32_t d = tmem + 256 + t * 128;
-        const uint32_t a_tm = tmem + t * 128;
+      }
+      __syncwarp();
+      commit(L::bSFull + t);
+    };
+    auto issue_pv = [=](int t, int slot, bool accumulate) {
+      const uint32_t d = tmem + 256 + t * 128;
+      const uint32_t a_tm = tmem + t * 128;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t b = smem_desc_sw128(ring_base + slot * kTileBytes + k * 2048, kPanelBytes, 1024);
+          const uint64_t b = v_desc + ((slot * kTileBytes + k * 2048) >> 4);
           mma_ts(d, a_tm + k * 8, b, kIdescO, (accumulate || k > 0) ? 1u : 0u);
         }
-      };
-      // K of key tile j sits in ring use 2j, V in ring use 2j + 1.
-      if (ok && n_iter > 0) {
-        ok = lane_wait(&bars[L::bRingFull + 0], 0, ab, p.err);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, 0);
-          issue_s(1, 0);
-          mma_commit(&bars[L::bRingEmpty + 0]);
-        }
       }
-      for (int j = 0; j < n_iter && ok; ++j) {
-        const bool last = (j + 1 == n_iter);
-        const int rv = 2 * j + 1, sv = rv % L::NS;
-        const int rk = 2 * j + 2, sk = rk % L::NS;
-        if (!lane_wait(&bars[L::bRingFull + sv], (rv / L::NS) & 1, ab, p.err) ||
-            !lane_wait(&bars[L::bPFull + 0], j & 1, ab, p.err)) {
-          ok = false;
-          break;
-        }
+      __syncwarp();
+
+    };
+    // K of key tile j sits in ring use 2j, V in ring use 2j + 1.
+    if (ok && n_iter > 0) {
+      ok = warp_wait(&bars[L::bRingFull + 0], 0, ab, p.err);
+      if (ok) {
         tc_fence_after();
-        issue_pv(0, sv, j > 0);
-        if (last) mma_commit(&bars[L::bPVDone + 0]);
-        if (!last) {
-          if (!lane_wait(&bars[L::bRingFull + sk], (rk / L::NS) & 1, ab, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_s(0, sk);
-        }
-        if (!lane_wait(&bars[L::bPFull + 1], j & 1, ab, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(1, sv, j > 0);
-        mma_commit(&bars[L::bRingEmpty + sv]);
-        if (last) {
-          mma_commit(&bars[L::bPVDone + 1]);
-        } else {
-          issue_s(1, sk);
-          mma_commit(&bars[L::bRingEmpty + sk]);
-        }
+        issue_s(0, 0);
+        issue_s(1, 0);
+        commit(L::bRingEmpty + 0);
       }
-      // Drain: all MMAs issued by this thread complete before tensor memory is freed.
-      mma_commit(&bars[L::bFinal]);
-      lane_wait_teardown(&bars[L::bFinal], 0, ok ? 2000000000ull : 20000000ull);
     }
-    __syncwarp();
+    for (int j = 0; j < n_iter && ok; ++j) {
+      const bool last = (j + 1 == n_iter);
+      const int rv = 2 * j + 1, sv = rv % L::NS;
+      const int rk = 2 * j + 2, sk = rk % L::NS;
+      if (!warp_wait(&bars[L::bRingFull + sv], (rv / L::NS) & 1, ab, p.err) ||
+          !warp_wait(&bars[L::bPFull + 0], j & 1, ab, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv(0, sv, j > 0);
+      if (last) commit(L::bPVDone + 0);
+      if (!last) {
+        if (!warp_wait(&bars[L::bRingFull + sk], (rk / L::NS) & 1, ab, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(0, sk);
+      }
+      if (!warp_wait(&bars[L::bPFull + 1], j & 1, ab, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv(1, sv, j > 0);
+      commit(L::bRingEmpty + sv);
+      if (last) {
+        commit(L::bPVDone + 1);
+      } else {
+        issue_s(1, sk);
+        commit(L::bRingEmpty + sk);
+      }
+    }
+    // Drain: all MMAs issued by this warp complete before tensor memory is freed.
+    commit(L::bFinal);
+    warp_wait_teardown(&bars[L::bFinal], 0, ok ? 2000000000ull : 20000000ull);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     // One thread per query row.  Per key tile: the whole 128-column score row

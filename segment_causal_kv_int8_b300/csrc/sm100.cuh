@@ -138,6 +138,20 @@ __device__ __forceinline__ bool warp_wait_teardown(uint64_t* bar, uint32_t parit
   }
 }
 
+// One lane of the (fully active) warp is elected; the others get false.  Code
+// that the whole warp executes keeps its operands in uniform registers, which
+// makes the elected lane's tcgen05.mma issue much cheaper than issue from a
+// divergent single-lane branch.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
