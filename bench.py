@@ -245,17 +245,24 @@ def run_ours(args):
         flush.zero_()
         flush.view(torch.int32).sum()
 
-    def step(ev_a0=None, ev_a1=None):
+    def step(ev=None):
+        # ev: None or 6 events bracketing append, RoPE and attention
         cache.reset(zero_memory=False)
+        if ev is not None:
+            ev[0].record(stream)
         for kh, vh in hist_d:
             cache.append(kh, vh)
+        if ev is not None:
+            ev[1].record(stream)
+            ev[2].record(stream)
         nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
-        if ev_a0 is not None:
-            ev_a0.record(stream)
+        if ev is not None:
+            ev[3].record(stream)
+            ev[4].record(stream)
         nomas.segment_attn(cache, 0, q, k, v, wl.n_video, wl.n_text, out=out, lse=lse, workspace=ws,
                            num_splits=args.num_splits)
-        if ev_a1 is not None:
-            ev_a1.record(stream)
+        if ev is not None:
+            ev[5].record(stream)
 
     def restage():
         q.copy_(q0)  # RoPE works in place: fresh un-rotated inputs for every step (untimed)
@@ -267,26 +274,29 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(dev.index if world == 1 else local)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
-    # Steps are enqueued back to back (one synchronisation after the last), so
-    # the host runs ahead of the GPU and no launch latency lands between the
-    # events.  Each step is bracketed by its own events; the L2 flush and the
-    # restaging copy sit between steps, outside them.
+    # Steps are enqueued back to back (one synchronisation after the last).  A
+    # GPU-side sleep queued first holds the stream while the host enqueues all
+    # steps, so no host launch latency lands between a step's events.  Each
+    # step is bracketed by its own events; the L2 flush and the restaging copy
+    # sit between steps, outside them, and the sleep precedes the first step.
+    torch.cuda._sleep(int(2e6) * args.steps)
     for i in range(args.steps):
         evict_l2()  # untimed, between steps
         restage()
-        e0, e1, a0, a1 = evs[i]
-        e0.record(stream)
-        step(a0, a1)
-        e1.record(stream)
+        evs[i][0].record(stream)
+        step(evs[i][2:])
+        evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    step_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in evs]
-    attn_ms = [a0.elapsed_time(a1) for _, _, a0, a1 in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    append_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    rope_ms = [e[4].elapsed_time(e[5]) for e in evs]
+    attn_ms = [e[6].elapsed_time(e[7]) for e in evs]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -309,6 +319,18 @@ def run_ours(args):
     launches_per_step = len(hist) + 1 + 1 + (1 if splits_used > 1 else 0)
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    in_esz = 2 if wl.io_dtype == "bf16" else 4
+    rope_bytes = wl.n_video * wl.heads * wl.head_dim * in_esz * 2 * 2  # Q and K, read + write
+    row_bytes = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if wl.cache_dtype == "int8" else 2 * wl.head_dim))
+    append_bytes = sum(min(f, wl.window) for f in wl.cache_frames_hist) * wl.tpf * wl.heads * row_bytes
+    elementwise = {}
+    for name, nbytes, ms in (("kvcache_append", append_bytes, append_ms), ("rope3d", rope_bytes, rope_ms)):
+        t = statistics.mean(ms)
+        gbs = nbytes / (t * 1e-3) / 1e9 if t > 0 else None
+        elementwise[name] = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": 1e3 * t, "achieved": gbs,
+                             "peak": hbm, "unit": "GB/s", "frac": gbs / hbm if gbs else None,
+                             "launches_per_step": len(hist) if name == "kvcache_append" else 1}
     traffic = _load_traffic(args.config)
     if rank == 0:
         line = {
@@ -321,6 +343,7 @@ def run_ours(args):
                          "kernel": "segment_attn_kernel" + (" + combine" if splits_used > 1 else ""),
                          "attn_ms": attn_avg, "splits": splits_used,
                          "peak_source": f"bf16_tflops (burst) of {src} peaks"},
+            "elementwise": elementwise,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,

@@ -35,7 +35,7 @@ struct AppendParams {
   int tpf;
   int first_frame;               // first segment frame written
   int n_tokens;                  // tokens written = (n_frames - first_frame) * tpf
-  long long total_before;        // absolute frames appended before this call
+  int base_slot_frame;           // ring frame-slot of the first written frame
   int capacity_frames;
   long long cap_slots;           // capacity_frames * tpf
   void* ck;                      // cache K (int8 or bf16)

@@ -10,8 +10,8 @@
 // One row = the head_dim = 128 values of one (tensor, block, head, token).
 // 16 threads own a row (8 values each: a 16-byte bf16 or 32-byte f32 load),
 // reduce the absmax with four shuffles and write 8 code bytes each plus the
-// row's scale.  Consecutive rows of a CTA are consecutive tokens of one
-// (block, head), so the code and scale stores of a CTA are contiguous.
+// row's scale.  A CTA covers a few consecutive tokens of 16 heads, so it reads
+// whole token rows and writes runs of consecutive ring slots per head.
 //
 // Codec bits (identical to the reference definition): scale = fl32(m / 127),
 // inv = fl32(127 / m) (IEEE round-to-nearest divisions), code =
@@ -44,59 +44,75 @@ __device__ __forceinline__ void load8(const void* base, long long off, float (&x
   }
 }
 
+constexpr int kAppendTokens = 4;  // tokens per block (and rows per 16-lane group)
+
+// Grid: x = groups of kAppendTokens tokens, y = groups of 16 heads, z = (block,
+// tensor).  16 lanes own one (token, head) row, 8 values each; the 16 row
+// groups of a CTA are 16 consecutive heads, so a CTA reads whole token rows
+// ([heads][128] contiguous in the input) and writes, per head, kAppendTokens
+// consecutive ring slots.  Each lane group issues all its loads before any
+// arithmetic.
 template <bool kF32In, bool kInt8>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
-  const long long per_tensor = static_cast<long long>(p.blocks) * p.heads * p.n_tokens;
-  const long long row = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
-  if (row >= 2 * per_tensor) return;  // whole 16-lane groups leave together
+  const int h = blockIdx.y * 16 + (threadIdx.x >> 4);
+  if (h >= p.heads) return;  // whole 16-lane groups leave together
   const int g = threadIdx.x & 15;
   const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
-  const int tensor = row >= per_tensor ? 1 : 0;
-  const long long rr = row - tensor * per_tensor;
-  const int n = static_cast<int>(rr % p.n_tokens);
-  const long long bhi = rr / p.n_tokens;
-  const int h = static_cast<int>(bhi % p.heads);
-  const int b = static_cast<int>(bhi / p.heads);
-  const int fs = p.first_frame + n / p.tpf;
-  const int within = n % p.tpf;
-  const long long slot = ((p.total_before + fs) % p.capacity_frames) * p.tpf + within;
-  const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
-  const long long src_off = b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g;
-  float x[8];
-  load8<kF32In>(tensor ? p.v : p.k, src_off, x);
-  const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots + slot;
-  if constexpr (kInt8) {
-    float m = 0.0f;
+  const int tensor = blockIdx.z & 1;
+  const int b = blockIdx.z >> 1;
+  const int n0 = blockIdx.x * kAppendTokens;
+  const void* src = tensor ? p.v : p.k;
+  const long long plane = static_cast<long long>(b) * p.heads + h;  // cache [block][head] plane
+  float x[kAppendTokens][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
-    const float scale = __fdiv_rn(m, 127.0f);
-    const float inv = __fdiv_rn(127.0f, m);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      int c = __float2int_rn(__fmul_rn(x[e], inv));
-      c = max(-127, min(127, c));
-      const uint32_t byte = static_cast<uint32_t>(c) & 0xFFu;
-      if (e < 4)
-        lo |= byte << (8 * e);
-      else
-        hi |= byte << (8 * (e - 4));
+  for (int r = 0; r < kAppendTokens; ++r) {
+    const int n = n0 + r;
+    if (n < p.n_tokens) {
+      const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
+      load8<kF32In>(src, b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g, x[r]);
     }
-    int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-    if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
-  } else {
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
-    uint4 w;
-    uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat162 t = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-      u[e] = *reinterpret_cast<const uint32_t*>(&t);
+  for (int r = 0; r < kAppendTokens; ++r) {
+    const int n = n0 + r;
+    if (n >= p.n_tokens) break;
+    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    int slot_frame = p.base_slot_frame + f;
+    if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
+    const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
+    if constexpr (kInt8) {
+      float m = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[r][e]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
+      const float scale = __fdiv_rn(m, 127.0f);
+      const float inv = __fdiv_rn(127.0f, m);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int c = __float2int_rn(__fmul_rn(x[r][e], inv));
+        c = max(-127, min(127, c));
+        const uint32_t byte = static_cast<uint32_t>(c) & 0xFFu;
+        if (e < 4)
+          lo |= byte << (8 * e);
+        else
+          hi |= byte << (8 * (e - 4));
+      }
+      int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
+      *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+      if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
+    } else {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
+      uint4 w;
+      uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 t = __floats2bfloat162_rn(x[r][2 * e], x[r][2 * e + 1]);
+        u[e] = *reinterpret_cast<const uint32_t*>(&t);
+      }
+      *reinterpret_cast<uint4*>(dst) = w;
     }
-    *reinterpret_cast<uint4*>(dst) = w;
   }
 }
 
@@ -112,21 +128,20 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint8_t* __restrict__ pt
 }  // namespace
 
 cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, cudaStream_t stream) {
-  const long long rows = 2LL * p.blocks * p.heads * p.n_tokens;
-  if (rows <= 0) return cudaSuccess;
-  const long long blocks = (rows + 15) / 16;
-  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  const unsigned nb = static_cast<unsigned>(blocks);
+  if (p.n_tokens <= 0 || p.blocks <= 0 || p.heads <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
+                  static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
+  if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
   if (f32_in) {
     if (int8_cache)
-      append_kernel<true, true><<<nb, 256, 0, stream>>>(p);
+      append_kernel<true, true><<<grid, 256, 0, stream>>>(p);
     else
-      append_kernel<true, false><<<nb, 256, 0, stream>>>(p);
+      append_kernel<true, false><<<grid, 256, 0, stream>>>(p);
   } else {
     if (int8_cache)
-      append_kernel<false, true><<<nb, 256, 0, stream>>>(p);
+      append_kernel<false, true><<<grid, 256, 0, stream>>>(p);
     else
-      append_kernel<false, false><<<nb, 256, 0, stream>>>(p);
+      append_kernel<false, false><<<grid, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }

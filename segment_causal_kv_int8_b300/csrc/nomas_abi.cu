@@ -280,7 +280,7 @@ NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k,
     p.tpf = static_cast<int>(tpf);
     p.first_frame = first;
     p.n_tokens = static_cast<int>(n_tokens);
-    p.total_before = cache->total_frames;
+    p.base_slot_frame = slot_frame;
     p.capacity_frames = cache->capacity_frames;
     p.cap_slots = tpf * cache->capacity_frames;
     p.ck = cache->k;

@@ -6,9 +6,9 @@
 // axis a rotates by pos_a * f_{a,i}, f_{a,i} = theta^(-2i/d_a).
 //
 // HBM-bound elementwise kernel: 16 threads own one token, each thread four
-// consecutive pairs (one 16-byte bf16 vector or two float4 of every head row).
-// The cos/sin of a (token, pair) is computed once and applied to all heads of
-// Q and K.  The angle pos * f is formed as a two-float product (f = f_hi +
+// consecutive pairs (one 16-byte bf16 vector or two float4 of a head row) of a
+// group of heads.  The cos/sin of a (token, pair) is computed once per head
+// group and applied to those heads of Q and K.  The angle pos * f is formed as a two-float product (f = f_hi +
 // f_lo, exact product error by fma) and reduced by the nearest multiple of
 // 2*pi with a three-float 2*pi (Cody-Waite reduction with fma), so the angle
 // error stays ~1e-7 rad at any frame index below 2^24; sincosf then sees |r|
@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 
@@ -37,17 +39,56 @@ __device__ __forceinline__ float reduced_angle(float pos, float f_hi, float f_lo
   return r + a_lo;
 }
 
+constexpr int kRopeHeadsPerThread = 4;
+
+// Rotate one 8-value group (4 pairs) held as floats.
+__device__ __forceinline__ void rotate8(float (&x)[8], const float (&cs)[4], const float (&sn)[4]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float x0 = x[2 * e], x1 = x[2 * e + 1];
+    x[2 * e] = fmaf(x0, cs[e], -x1 * sn[e]);
+    x[2 * e + 1] = fmaf(x0, sn[e], x1 * cs[e]);
+  }
+}
+
+// Block: 16 tokens x 16 lanes (a lane owns 4 consecutive rotary pairs, i.e. 8
+// values, of every head row); blockIdx.y picks a group of kRopeHeadsPerThread
+// heads.  All loads of a thread (its heads of Q and K) are issued before any
+// arithmetic so enough bytes are in flight to keep HBM busy.
 template <bool kBF16>
 __global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void* __restrict__ k,
                                                      const __grid_constant__ RopeParams p, TwoPi tp) {
+  constexpr int HT = kRopeHeadsPerThread;
   const int g = threadIdx.x & 15;
-  const long long tok = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int tok = blockIdx.x * 16 + (threadIdx.x >> 4);
   if (tok >= p.n_video) return;
-  const int within = static_cast<int>(tok % p.tpf);
-  const float pos[3] = {static_cast<float>(p.t0 + tok / p.tpf), static_cast<float>(within / p.grid_w),
-                        static_cast<float>(within % p.grid_w)};
-  float cs[4], sn[4];
+  const int h0 = blockIdx.y * HT;
+  const int nh = min(HT, p.heads - h0);
   bool any = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) any |= p.axis[4 * g + e] >= 0;
+  if (!any) return;
+  const int nt = (k != nullptr) ? 2 : 1;
+  using Vec = typename std::conditional<kBF16, uint4, float4>::type;
+  constexpr int kVecs = kBF16 ? 1 : 2;  // 16-byte vectors per 8-value group
+  Vec w[2][HT][kVecs];
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    if (which >= nt) break;
+    const Vec* row = reinterpret_cast<const Vec*>(static_cast<const char*>(which ? k : q) +
+                                                  (static_cast<long long>(tok) * p.row_stride + h0 * 128 + 8 * g) * (kBF16 ? 2 : 4));
+#pragma unroll
+    for (int u = 0; u < HT; ++u)
+      if (u < nh)
+#pragma unroll
+        for (int c = 0; c < kVecs; ++c) w[which][u][c] = row[u * (128 * (kBF16 ? 2 : 4) / 16) + c];
+  }
+  const int frame = tok / p.tpf;
+  const int within = tok - frame * p.tpf;
+  const int row = within / p.grid_w;
+  const float pos[3] = {static_cast<float>(p.t0 + frame), static_cast<float>(row),
+                        static_cast<float>(within - row * p.grid_w)};
+  float cs[4], sn[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int pair = 4 * g + e;
@@ -56,60 +97,43 @@ __global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void*
       cs[e] = 1.0f;
       sn[e] = 0.0f;
     } else {
-      any = true;
       sincosf(reduced_angle(pos[a], p.f_hi[pair], p.f_lo[pair], tp), &sn[e], &cs[e]);
     }
   }
-  if (!any) return;
+#pragma unroll
   for (int which = 0; which < 2; ++which) {
-    void* base = which ? k : q;
-    if (base == nullptr) continue;
-    if constexpr (kBF16) {
-      __nv_bfloat16* row = static_cast<__nv_bfloat16*>(base) + tok * p.row_stride + 8 * g;
-      for (int h0 = 0; h0 < p.heads; h0 += 4) {
-        uint4 w[4];
+    if (which >= nt) break;
+    Vec* row = reinterpret_cast<Vec*>(static_cast<char*>(which ? k : q) +
+                                      (static_cast<long long>(tok) * p.row_stride + h0 * 128 + 8 * g) * (kBF16 ? 2 : 4));
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (h0 + u < p.heads) w[u] = *reinterpret_cast<const uint4*>(row + (h0 + u) * 128);
+    for (int u = 0; u < HT; ++u) {
+      if (u >= nh) continue;
+      float x[8];
+      if constexpr (kBF16) {
+        const uint32_t* v = reinterpret_cast<const uint32_t*>(&w[which][u][0]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (h0 + u >= p.heads) continue;
-          uint32_t* x = reinterpret_cast<uint32_t*>(&w[u]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&x[e]);
-            const float x0 = __bfloat162float(v2.x), x1 = __bfloat162float(v2.y);
-            const float y0 = fmaf(x0, cs[e], -x1 * sn[e]);
-            const float y1 = fmaf(x0, sn[e], x1 * cs[e]);
-            __nv_bfloat162 o2 = __floats2bfloat162_rn(y0, y1);
-            x[e] = *reinterpret_cast<const uint32_t*>(&o2);
-          }
-          *reinterpret_cast<uint4*>(row + (h0 + u) * 128) = w[u];
+        for (int e = 0; e < 4; ++e) {
+          x[2 * e] = __uint_as_float(v[e] << 16);
+          x[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
         }
+      } else {
+        const float* v = reinterpret_cast<const float*>(&w[which][u][0]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = v[e];
       }
-    } else {
-      float* row = static_cast<float*>(base) + tok * p.row_stride + 8 * g;
-      for (int h0 = 0; h0 < p.heads; h0 += 2) {
-        float4 w[2][2];
+      rotate8(x, cs, sn);
+      if constexpr (kBF16) {
+        uint4 o;
+        uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
-          if (h0 + u < p.heads) {
-            w[u][0] = *reinterpret_cast<const float4*>(row + (h0 + u) * 128);
-            w[u][1] = *reinterpret_cast<const float4*>(row + (h0 + u) * 128 + 4);
-          }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (h0 + u >= p.heads) continue;
-          float* x = reinterpret_cast<float*>(&w[u][0]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = x[2 * e], x1 = x[2 * e + 1];
-            x[2 * e] = fmaf(x0, cs[e], -x1 * sn[e]);
-            x[2 * e + 1] = fmaf(x0, sn[e], x1 * cs[e]);
-          }
-          *reinterpret_cast<float4*>(row + (h0 + u) * 128) = w[u][0];
-          *reinterpret_cast<float4*>(row + (h0 + u) * 128 + 4) = w[u][1];
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 t2 = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+          ov[e] = *reinterpret_cast<const uint32_t*>(&t2);
         }
+        row[u * 16] = o;
+      } else {
+        row[u * 32] = make_float4(x[0], x[1], x[2], x[3]);
+        row[u * 32 + 1] = make_float4(x[4], x[5], x[6], x[7]);
       }
     }
   }
@@ -129,12 +153,14 @@ TwoPi two_pi_split() {
 
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream) {
   if (p.n_video <= 0) return cudaSuccess;
-  const unsigned blocks = static_cast<unsigned>((p.n_video + 15) / 16);
+  const dim3 grid(static_cast<unsigned>((p.n_video + 15) / 16),
+                  static_cast<unsigned>((p.heads + kRopeHeadsPerThread - 1) / kRopeHeadsPerThread));
+  if (grid.y > 65535) return cudaErrorInvalidValue;
   const TwoPi tp = two_pi_split();
   if (bf16_io)
-    rope3d_kernel<true><<<blocks, 256, 0, stream>>>(q, k, p, tp);
+    rope3d_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp);
   else
-    rope3d_kernel<false><<<blocks, 256, 0, stream>>>(q, k, p, tp);
+    rope3d_kernel<false><<<grid, 256, 0, stream>>>(q, k, p, tp);
   return cudaGetLastError();
 }
 
