@@ -68,6 +68,28 @@ def dist_env():
     return rank, world, local
 
 
+# ------------------------------------------------------------------ multi-rank host logic
+def rank_block(rank: int) -> int:
+    """Seed block of a rank: every rank runs an independent block's workload (no data exchange)."""
+    return rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Maximum of a per-rank timing over all ranks (the job ends when the slowest rank does)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_step: float, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of all ranks' timed steps over the slowest rank's time."""
+    return flops_per_step * world * steps / (total_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 def oracle_sample(wl, seconds: float, block: int = 0):
     """Time the oracle's RoPE + segment attention on a sample of query rows.
@@ -217,7 +239,7 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     wl = CONFIGS[args.config]
-    block = rank  # each rank owns an independent block's data
+    block = rank_block(rank)  # each rank owns an independent block's data
 
     # ---- synthetic inputs (seeded), resident in HBM before timing
     hist = history_segments(wl, block)
@@ -301,14 +323,10 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     flops = wl.attn_flops()
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_value(flops, world, args.steps, total_ms)
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
 
@@ -425,24 +443,47 @@ def _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ms.append(e0.elapsed_time(e1))
-    total = sum(ms)
-    if world > 1:
-        t = torch.tensor([total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-    val = wl.attn_flops() * world * args.steps / (total * 1e-3) / 1e12
+    total = max_over_ranks(sum(ms), world, dev)
+    val = whole_job_value(wl.attn_flops(), world, args.steps, total)
     return {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": total / args.steps}
 
 
+ATTN_SOURCES = ("segment_causal_kv_int8_b300/csrc/segment_attn.cu", "segment_causal_kv_int8_b300/csrc/sm100.cuh")
+
+
+def attn_source_hash() -> str:
+    """sha256 over the attention kernel's sources (decides whether committed counters still apply)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _load_traffic(config):
-    """DRAM bytes per attention launch from a committed ncu summary, if one matches the current kernel."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{config}.json")
+    """DRAM bytes per attention launch from the committed ncu summary of this config.
+
+    ``profiles/attention_<config>.md`` records ``dram_bytes_per_launch`` and the
+    ``kernel_source_sha256`` of the sources it was captured from; the value is
+    used only while the sources still hash the same, else traffic is null.
+    """
+    path = os.path.join(ROOT, "profiles", f"attention_{config}.md")
+    fields = {}
     try:
         with open(path) as f:
-            d = json.load(f)
-        return d.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+            for line in f:
+                if ":" in line:
+                    k, _, v = line.strip().lstrip("-* `").partition(":")
+                    fields[k.strip(" `")] = v.strip(" `")
+    except OSError:
+        return None
+    if fields.get("kernel_source_sha256") != attn_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
         return None
 
 

@@ -229,6 +229,16 @@ nomas_status nomas_segment_attn_noalloc(const nomas_kvcache* cache, int32_t bloc
 nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream);
 
 /*
+ * Self-test of the bounded-wait error path (no counterpart in the pages):
+ * enqueue a one-warp kernel that waits up to limit_us microseconds (1 ..
+ * 2,000,000) on an on-chip barrier that nothing arrives on, then records
+ * NOMAS_ERR_DEVICE_TIMEOUT in the device error word and exits normally.  No
+ * fault or hang is involved; the context stays usable.  Read the result with
+ * nomas_device_error.  Returns NOMAS_ERR_INVALID_ARG for a limit out of range.
+ */
+nomas_status nomas_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
+/*
  * Read the device-side error word of the current device (a status code set
  * by a kernel that gave up waiting, 0 if none), synchronously.  With clear != 0
  * the word is reset to 0.  *status receives NOMAS_OK or the recorded status.

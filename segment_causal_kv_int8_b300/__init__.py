@@ -83,6 +83,7 @@ EXPORTS = {
     "nomas_segment_attn_noalloc": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
                                             _i32, _vp]),
     "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
+    "nomas_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _vp]),
     "nomas_device_error": (_c_int, [_P(_c_int), _c_int]),
 }
 

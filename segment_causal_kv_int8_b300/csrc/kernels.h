@@ -49,6 +49,9 @@ cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, c
 // ------------------------------------------------------------------ reset
 cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);
 
+// ------------------------------------------------------------------ self-test
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
+
 // ------------------------------------------------------------------ attention
 struct AttnTensorMaps {
   CUtensorMap q, kcur, vcur, kc, vc;

@@ -409,6 +409,14 @@ NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t bl
   return st;
 }
 
+NOMAS_API nomas_status nomas_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return NOMAS_ERR_INVALID_ARG;
+  uint32_t* err = nullptr;
+  nomas_status st = device_state(&err, nullptr);
+  if (st != NOMAS_OK) return st;
+  return from_cuda(launch_wait_timeout_selftest(err, static_cast<uint64_t>(limit_us) * 1000ull, stream));
+}
+
 NOMAS_API nomas_status nomas_device_error(nomas_status* status, int clear) {
   if (status == nullptr) return NOMAS_ERR_INVALID_ARG;
   uint32_t* err = nullptr;

@@ -1,0 +1,37 @@
+// selftest.cu - a kernel that exercises the bounded-wait error path.
+//
+// Every wait of the library's kernels on an mbarrier gives up after a time
+// limit, records NOMAS_ERR_DEVICE_TIMEOUT in the device error word and
+// returns, so a lost arrival never hangs the GPU.  This kernel waits, with the
+// caller's limit, on a barrier that nothing ever arrives on, which takes that
+// path on purpose without any fault: the wait ends by the clock, the error word
+// is set, and the kernel exits normally.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace nomas {
+namespace {
+
+__global__ void __launch_bounds__(32) wait_timeout_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ AbortState ab;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);  // expects one arrival that never comes
+    ab.flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+  warp_wait_limit(&bar, 0, &ab, err, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace nomas

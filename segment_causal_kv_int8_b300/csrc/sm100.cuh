@@ -65,8 +65,8 @@ constexpr uint32_t kErrTimeout = 5u;               // NOMAS_ERR_DEVICE_TIMEOUT
 // All 32 lanes must call it together.  Returns false (for all lanes) if the
 // CTA is aborting or the wait exceeded kWaitLimitNs; in the latter case the
 // device error word is set and the CTA's abort flag raised.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortState* ab,
-                                          uint32_t* err_word) {
+__device__ __forceinline__ bool warp_wait_limit(uint64_t* bar, uint32_t parity, AbortState* ab,
+                                                uint32_t* err_word, uint64_t limit_ns) {
   const uint32_t addr = smem_u32(bar);
   uint32_t ok = mbar_try_wait(addr, parity);
   if (__all_sync(0xffffffffu, ok)) return true;
@@ -80,7 +80,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortS
       if ((threadIdx.x & 31) == 0) {
         if (ab->flag) {
           give_up = 1;
-        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+        } else if (global_timer_ns() - t0 > limit_ns) {
           give_up = 1;
           ab->flag = 1;
           if (err_word) atomicCAS(err_word, 0u, kErrTimeout);
@@ -90,6 +90,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortS
       if (give_up) return false;
     }
   }
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, AbortState* ab, uint32_t* err_word) {
+  return warp_wait_limit(bar, parity, ab, err_word, kWaitLimitNs);
 }
 
 // Single-thread bounded wait (for roles that run on one elected lane).  Same

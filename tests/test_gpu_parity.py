@@ -222,3 +222,17 @@ def test_invalid_arguments_launch_nothing():
     with pytest.raises(nomas.NomasError) as e:
         nomas.segment_attn(gc, 0, q, q, q, wl.n_video, wl.n_text, num_splits=3)   # no workspace
     assert e.value.status == nomas.NOMAS_ERR_INVALID_ARG
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    # A kernel waits on a barrier nothing arrives on; after 50 ms it records the
+    # timeout status and exits.  The context must stay usable afterwards.
+    assert nomas.device_error(clear=True) == 0
+    st = nomas.nomas_selftest_wait_timeout(50_000, nomas._stream_ptr())
+    assert st == nomas.NOMAS_OK
+    torch.cuda.synchronize()
+    assert nomas.device_error(clear=True) == nomas.NOMAS_ERR_DEVICE_TIMEOUT
+    assert nomas.device_error(clear=False) == 0
+    assert nomas.nomas_selftest_wait_timeout(0, nomas._stream_ptr()) == nomas.NOMAS_ERR_INVALID_ARG
+    x = torch.arange(16, device="cuda", dtype=torch.float32)
+    assert float(x.sum()) == 120.0
