@@ -373,11 +373,12 @@ NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t bl
   const uint64_t bh_rows = static_cast<uint64_t>(cache->num_blocks) * H;
   if (st == NOMAS_OK && pl.nc > 0) {
     if (int8) {
+      // Each CTA of an INT8 pair stages half a tile: boxes of 64 rows.
       st = encode3d(&tm.kc, CU_TENSOR_MAP_DATA_TYPE_UINT8, cache->k, 128, pl.nc, bh_rows, 128, cap_slots * 128, 128,
-                    128, 1);
+                    64, 1);
       if (st == NOMAS_OK)
         st = encode3d(&tm.vc, CU_TENSOR_MAP_DATA_TYPE_UINT8, cache->v, 128, pl.nc, bh_rows, 128, cap_slots * 128, 128,
-                      128, 1);
+                      64, 1);
     } else {
       st = encode3d(&tm.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache->k, 128, pl.nc, bh_rows, 256, cap_slots * 256, 64,
                     128, 1);

@@ -42,7 +42,8 @@ namespace attn {
 constexpr int kThreads = 512;
 constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 tile: [2 panels][128 rows][128 B]
 constexpr int kPanelBytes = 128 * 128;      // 64 bf16 columns x 128 rows, 128B-swizzled
-constexpr int kI8TileBytes = 128 * 128;     // one int8 tile: [128 rows][128 B], 128B-swizzled
+constexpr int kI8HalfBytes = 64 * 128;      // one CTA's half of an int8 tile: [64 rows][128 B], 128B-swizzled
+constexpr int kHalfPanelBytes = 64 * 128;   // 64 rows of one bf16 panel (one CTA's half of it)
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // S = Q K^T (both K-major)
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, true);   // O += P V (V is N-major)
 constexpr float kLazyRescale = 8.0f;        // log2 of the tolerated growth of exp terms
@@ -56,19 +57,20 @@ constexpr uint32_t kFillerRegs = 72;    // warps 12-15: INT8 ring fillers
 
 template <bool kInt8>
 struct Layout {
-  static constexpr int NS = kInt8 ? 3 : 5;  // bf16 ring slots (K and V tiles alternate)
-  static constexpr int NI = kInt8 ? 3 : 0;  // int8 staging slots
+  static constexpr int NS = kInt8 ? 4 : 5;  // bf16 ring slots (K and V tiles alternate)
+  static constexpr int NI = kInt8 ? 4 : 0;  // int8 staging slots (half tiles)
   static constexpr int kQ = 0;
   static constexpr int kRing = 2 * kTileBytes;
   static constexpr int kStage = kRing + NS * kTileBytes;
-  static constexpr int kBars = kStage + NI * kI8TileBytes;
+  static constexpr int kBars = kStage + NI * kI8HalfBytes;
   // barrier indices
   static constexpr int bQ = 0;
   static constexpr int bRingFull = 1;
   static constexpr int bRingEmpty = bRingFull + NS;
   static constexpr int bStageFull = bRingEmpty + NS;
   static constexpr int bStageEmpty = bStageFull + NI;
-  static constexpr int bSFull = bStageEmpty + NI;  // [2]
+  static constexpr int bHalfReady = bStageEmpty + NI;  // [NI] INT8: this CTA's half tile is in its ring
+  static constexpr int bSFull = bHalfReady + NI;   // [2]
   static constexpr int bPFull = bSFull + 2;         // [2]
   static constexpr int bPVDone = bPFull + 2;        // [2]
   static constexpr int bFinal = bPVDone + 2;
@@ -131,12 +133,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars[L::bQ], 1);
     for (int s = 0; s < L::NS; ++s) {
+      // INT8: one arrival per local filler warp, plus the transaction bytes
+      // of the partner's half tile; both CTAs' MMA warps release every slot
+      // (multicast commit).
       mbar_init(&bars[L::bRingFull + s], kInt8 ? 4 : 1);
-      mbar_init(&bars[L::bRingEmpty + s], 1);
+      mbar_init(&bars[L::bRingEmpty + s], kInt8 ? 2 : 1);
     }
     for (int s = 0; s < L::NI; ++s) {
       mbar_init(&bars[L::bStageFull + s], 1);
-      mbar_init(&bars[L::bStageEmpty + s], 4);
+      mbar_init(&bars[L::bStageEmpty + s], 4);  // one arrival per filler warp
+      mbar_init(&bars[L::bHalfReady + s], 4);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[L::bSFull + t], 1);
@@ -153,8 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // INT8: the pair's barriers must be initialised before either CTA signals the other.
+  if constexpr (kInt8) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t rank = kInt8 ? cluster_ctarank() : 0u;  // position in the CTA pair
 
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sRing = smem + L::kRing;
@@ -199,8 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             uint64_t* fb = &bars[L::bStageFull + si];
-            mbar_arrive_expect_tx(fb, kI8TileBytes);
-            tma_load_3d(sStage + si * kI8TileBytes, kv ? &tm_vc : &tm_kc, fb, 0, ti.row0, bh);
+            mbar_arrive_expect_tx(fb, kI8HalfBytes);
+            tma_load_3d(sStage + si * kI8HalfBytes, kv ? &tm_vc : &tm_kc, fb, 0, ti.row0 + 64 * static_cast<int>(rank),
+                        bh);
           }
           ++ri_done;
         } else {
@@ -259,6 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) mma_commit(&bars[bar]);
       __syncwarp();
     };
+    // A ring slot is released in both CTAs of an INT8 pair (both fill it).
+    auto release = [=](int bar) {
+      if (elect_one()) {
+        if constexpr (kInt8)
+          mma_commit_multicast(&bars[bar], 0x3);
+        else
+          mma_commit(&bars[bar]);
+      }
+      __syncwarp();
+    };
     auto issue_s = [=](int t, int slot) {
       const uint32_t d = tmem + t * 128;
       if (elect_one()) {
@@ -293,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
-        commit(L::bRingEmpty + 0);
+        release(L::bRingEmpty + 0);
       }
     }
     for (int j = 0; j < n_iter && ok; ++j) {
@@ -322,12 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       issue_pv(1, sv, j > 0);
-      commit(L::bRingEmpty + sv);
+      release(L::bRingEmpty + sv);
       if (last) {
         commit(L::bPVDone + 1);
       } else {
         issue_s(1, sk);
-        commit(L::bRingEmpty + sk);
+        release(L::bRingEmpty + sk);
       }
     }
     // Drain: all MMAs issued by this warp complete before tensor memory is freed.
@@ -476,34 +496,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ ring filler (INT8 cache)
-    // Fills every ring slot in order: int8 cache tiles are dequantised from
-    // the staging slots (x_hat = bf16(code * scale)), current-segment bf16
-    // tiles are fetched by TMA (issued by warp 12).  All four warps wait for
-    // the slot to be empty and arrive once on its full-barrier (count 4).
+    // The two CTAs of a pair work on the same head and key range (adjacent
+    // query blocks) and share every dequantised tile: each CTA dequantises
+    // its half (64 rows) of each int8 cache tile, x_hat = bf16(code * scale),
+    // into its own ring slot, and the copy engine then moves that half into
+    // the partner's slot (two 8 KB shared-to-shared bulk copies that complete
+    // transactions on the partner's full-barrier).  Current-segment bf16
+    // tiles are fetched by TMA into the local ring (issued by warp 12).  Each
+    // local filler warp arrives once on a slot's full-barrier (count 4), and a
+    // slot is reused only after both CTAs' MMA warps released it, so neither
+    // a copy nor a dequantising thread writes into a slot still being read.
     if constexpr (kInt8) {
-      const int drow = threadIdx.x - 384;  // 0..127: one tile row per thread
-      const int sw = drow & 7;
+      const int ft = threadIdx.x - 384;  // 0..127
+      const int hrow = ft >> 1;          // row of this CTA's half tile (0..63)
+      const int half = ft & 1;           // bf16 panel written: columns 64*half .. 64*half+63
+      const int trow = 64 * static_cast<int>(rank) + hrow;  // row of the 128-row tile
+      const int sw_src = hrow & 7, sw_dst = trow & 7;
+      const uint32_t peer = rank ^ 1u;
       int ri = 0, r_tma = 0;
       bool ok = true;
       for (int it = 0; it < n_iter && ok; ++it) {
         const TileInfo ti = tile_info(t_begin + it, p);
         for (int kv = 0; kv < 2; ++kv) {
           const int r = 2 * it + kv, s = r % L::NS, u = r / L::NS;
+          uint64_t* fb = &bars[L::bRingFull + s];
           if (!ti.cache) {
             if (u > 0 && !warp_wait(&bars[L::bRingEmpty + s], (u - 1) & 1, ab, p.err)) {
               ok = false;
               break;
             }
             if (lane == 0) {
-              uint64_t* fb = &bars[L::bRingFull + s];
               if (warp == 12) {
-                mbar_arrive_expect_tx(fb, kTileBytes);
+                mbar_expect_tx(fb, kTileBytes);
                 uint8_t* dst = sRing + s * kTileBytes;
                 for (int pn = 0; pn < 2; ++pn)
                   tma_load_3d(dst + pn * kPanelBytes, kv ? &tm_vcur : &tm_kcur, fb, pn * 64, head, ti.row0);
-              } else {
-                mbar_arrive(fb);
               }
+              mbar_arrive(fb);
             }
             r_tma = r + 1;
             __syncwarp();
@@ -512,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int si = ri % L::NI, ui = ri / L::NI;
           const float* sp = kv ? p.v_scale : p.k_scale;
           const float sc =
-              (drow < ti.valid) ? sp[static_cast<size_t>(bh) * p.scale_stride + ti.row0 + drow] : 0.0f;
+              (trow < ti.valid) ? sp[static_cast<size_t>(bh) * p.scale_stride + ti.row0 + trow] : 0.0f;
           if (!warp_wait(&bars[L::bStageFull + si], ui & 1, ab, p.err)) {
             ok = false;
             break;
@@ -521,11 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint8_t* src = sStage + si * kI8TileBytes + drow * 128;
-          uint8_t* dst = sRing + s * kTileBytes + drow * 128;
+          const uint8_t* src = sStage + si * kI8HalfBytes + hrow * 128;
+          uint8_t* dst = sRing + s * kTileBytes + half * kPanelBytes + trow * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = 4 * half + cc;  // int8 chunk: columns 16c .. 16c+15
+            const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw_src) << 4));
             const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
             uint32_t o[8];
 #pragma unroll
@@ -537,27 +567,53 @@ __global__ void __launch_bounds__(kThreads, 1)
               o[2 * e] = pack_bf16x2(f0, f1);
               o[2 * e + 1] = pack_bf16x2(f2, f3);
             }
-            // int8 columns 16c..16c+15 -> bf16 panel c/4, 16-byte chunks 2(c%4) and 2(c%4)+1
-            uint8_t* pd = dst + (c >> 2) * kPanelBytes;
-            const int c0 = (2 * (c & 3)) ^ sw, c1 = (2 * (c & 3) + 1) ^ sw;
-            *reinterpret_cast<uint4*>(pd + (c0 << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(pd + (c1 << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            // 16 int8 columns -> 16-byte chunks 2cc and 2cc+1 of bf16 panel `half`
+            *reinterpret_cast<uint4*>(dst + ((((2 * cc) ^ sw_dst)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + ((((2 * cc + 1) ^ sw_dst)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&bars[L::bRingFull + s]);
+            mbar_arrive(&bars[L::bHalfReady + si]);
+            if (warp == 12) {
+              // The partner's half arrives as 16 KB of transactions on this slot.
+              mbar_expect_tx(fb, 2 * kHalfPanelBytes);
+              // Once all four local warps wrote this CTA's half, copy it (64 rows
+              // of each 128-row panel, contiguous) into the partner's slot.
+              if (!lane_wait(&bars[L::bHalfReady + si], ui & 1, ab, p.err)) {
+                ok = false;
+              } else {
+                const uint32_t peer_fb = mapa_shared(smem_u32(fb), peer);
+                for (int pn = 0; pn < 2; ++pn) {
+                  const uint8_t* half_src = sRing + s * kTileBytes + pn * kPanelBytes + 64 * rank * 128;
+                  bulk_copy_to_cluster(mapa_shared(smem_u32(half_src), peer), half_src, kHalfPanelBytes,
+                                       peer_fb);
+                }
+              }
+            }
+            mbar_arrive(fb);
             mbar_arrive(&bars[L::bStageEmpty + si]);
           }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           ++ri;
         }
       }
       if (!ok && warp == 12) {
-        // Abort: wait for the current-tile copies this warp issued.
+        // Abort: give the current-tile copies this warp issued time to land.
         for (int r = r_tma - 1; r >= 0 && r >= r_tma - L::NS; --r) {
           const TileInfo ti = tile_info(t_begin + r / 2, p);
           if (ti.cache) continue;
           warp_wait_teardown(&bars[L::bRingFull + r % L::NS], (r / L::NS) & 1, 20000000ull);
+        }
+      }
+      if (warp == 12) {
+        // Both MMA warps release every slot in both CTAs: wait until the last
+        // release of each slot has arrived here, so no release is still in
+        // flight toward this CTA when the pair meets at the final barrier.
+        const int uses = 2 * n_iter;
+        for (int sl = 0; sl < L::NS && sl < uses; ++sl) {
+          const int n_s = (uses - sl + L::NS - 1) / L::NS;
+          warp_wait_teardown(&bars[L::bRingEmpty + sl], (n_s - 1) & 1, ok ? 2000000000ull : 20000000ull);
         }
       }
     }
@@ -565,6 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // INT8: neither CTA of a pair leaves while the other may still write into
+  // its shared memory or arrive on its barriers.
+  if constexpr (kInt8) cluster_sync();
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -616,8 +675,27 @@ static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, in
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  dim3 grid(n_pairs, p.heads, p.num_splits);
-  segment_attn_kernel<kInt8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
+  if constexpr (kInt8) {
+    // CTA pairs (clusters of two adjacent query blocks) share the dequantised
+    // tiles; an odd count gets one query block past the end (no live rows).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((n_pairs + 1) & ~1, p.heads, p.num_splits);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, segment_attn_kernel<kInt8>, tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
+    if (e != cudaSuccess) return e;
+  } else {
+    dim3 grid(n_pairs, p.heads, p.num_splits);
+    segment_attn_kernel<kInt8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
+  }
   return cudaGetLastError();
 }
 
