@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
     return ap.parse_args()
 
 
@@ -487,10 +488,119 @@ def _load_traffic(config):
         return None
 
 
+# ------------------------------------------------------------------ session workload
+def session_flops(wl, turns: int) -> float:
+    """Attention FLOPs of a session: every turn runs steps x blocks calls over the cache resident then."""
+    total = 0.0
+    for t in range(turns):
+        n_k = min(t * wl.cur_frames, wl.window) * wl.tpf + wl.n_q
+        total += wl.steps * wl.blocks * 4.0 * wl.n_q * n_k * wl.head_dim * wl.heads
+    return total
+
+
+def run_session(args):
+    """The simulated multi-turn session: per turn, steps x blocks calls of RoPE + segment attention
+    (each block against its own window of the shared INT8 cache), then one append of the finished
+    segment's K/V for all blocks.  One timed step = one whole session of ``--turns`` turns."""
+    import torch
+    import torch.distributed as dist
+
+    import segment_causal_kv_int8_b300 as nomas
+    from synth import CONFIGS, current_qkv_torch, segment_kv_torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    wl = CONFIGS[args.config]
+    turns = min(args.turns, wl.turns)
+    seed_block = rank_block(rank)
+    cache = nomas.KVCache(wl.blocks, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames,
+                          wl.cache_dtype, device=dev)
+    # A pool of current-segment inputs (values do not change the work) and one
+    # finished segment per turn, drawn on the device before timing.
+    pool = [current_qkv_torch(wl, seed_block, s, b, dev) for s, b in ((0, 0), (1, 1), (2, 2), (3, 3))]
+    seg_k, seg_v = segment_kv_torch(wl, seed_block, wl.cur_frames, wl.blocks, dev)
+    out = torch.empty_like(pool[0][0])
+    ws_bytes = 0
+    for vf in range(0, wl.window + 1):
+        d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
+        d.total_frames, d.valid_frames = vf, vf
+        import ctypes
+        b = ctypes.c_size_t()
+        nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), wl.n_video, wl.n_text, 0, ctypes.byref(b))
+        ws_bytes = max(ws_bytes, int(b.value))
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    calls = [0]
+
+    def session():
+        cache.reset(zero_memory=False)
+        for t in range(turns):
+            for s in range(wl.steps):
+                for blk in range(wl.blocks):
+                    q, k, v = pool[(s * wl.blocks + blk) % len(pool)]
+                    nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, cache.total_frames, wl.theta,
+                                 wl.rope_split)
+                    nomas.segment_attn(cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
+                    calls[0] += 2
+            cache.append(seg_k, seg_v)
+            calls[0] += 1
+
+    for _ in range(args.warmup):
+        session()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    calls[0] = 0
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        session()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
+    flops = session_flops(wl, turns)
+    value = whole_job_value(flops, world, args.steps, total_ms)
+    peaks, src = load_peaks()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {turns} turns x {wl.steps} steps x {wl.blocks} blocks of RoPE + "
+                                   f"segment attention ({wl.heads} heads x {wl.head_dim}, Nq={wl.n_q}, INT8 cache "
+                                   f"window {wl.window} frames), one 54-block append per turn; one step = one session",
+                       "turns": turns, "attention_calls": turns * wl.steps * wl.blocks,
+                       "l2": "working set (54 blocks' caches, input pool) far larger than L2",
+                       "parallelism": f"replica x{world} (independent sessions per GPU)"},
+            "roofline": {"bound": "tensor", "achieved": value / world, "peak": float(peaks["bf16_tflops_sustained"]),
+                         "unit": UNIT, "frac": value / world / float(peaks["bf16_tflops_sustained"]),
+                         "traffic": None, "kernel": "whole session (attention dominant)",
+                         "peak_source": f"bf16_tflops_sustained of {src} peaks (a seconds-long step)"},
+            "gpu_launches": calls[0], "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.config == "c5_session12":
+        return run_session(args)
     return run_ours(args)
 
 

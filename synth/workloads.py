@@ -192,3 +192,41 @@ def history_segments(wl: Workload, block: int = 0) -> List[Tuple[np.ndarray, np.
 def small_variant(wl: Workload, **changes) -> Workload:
     """A copy of ``wl`` with some fields replaced (used for ragged / edge shapes)."""
     return dataclasses.replace(wl, **changes)
+
+
+# ---------------------------------------------------------------- device-side draws
+# The session workload (54 blocks x 12 turns x 8 steps) is too large to draw
+# on the host for every call.  These draws use torch's counter-based
+# generator on the given device, seeded from the same integer tuples; they are
+# a different stream of numbers from the NumPy draws above, but serve the CUDA
+# path and the oracle alike (the oracle receives copies of them).
+def _torch_seed(*key: int) -> int:
+    ss = np.random.SeedSequence([int(k) for k in key])
+    return int(ss.generate_state(1, dtype=np.uint64)[0] & 0x7FFFFFFFFFFFFFFF)
+
+
+def _torch_normal(shape, seed: int, device, outlier_p: float, outlier_mag: float):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if outlier_p > 0.0:
+        hit = torch.rand(shape, generator=g, device=device) < outlier_p
+        sign = torch.where(torch.rand(shape, generator=g, device=device) < 0.5, -1.0, 1.0)
+        x = torch.where(hit, sign * outlier_mag, x)
+    return x.to(torch.bfloat16)
+
+
+def current_qkv_torch(wl: Workload, turn: int, step: int, block: int, device):
+    """Q, K, V of the current segment as bf16 tensors on ``device``, ``[n_q][heads][head_dim]``."""
+    shape = (wl.n_q, wl.heads, wl.head_dim)
+    return tuple(_torch_normal(shape, _torch_seed(wl.seed, tag, turn, step, block), device,
+                               0.0 if tag == _TAG_Q else wl.outlier_p, wl.outlier_mag)
+                 for tag in (_TAG_Q, _TAG_K, _TAG_V))
+
+
+def segment_kv_torch(wl: Workload, segment: int, frames: int, blocks: int, device):
+    """K and V of a finished segment for ``blocks`` blocks, bf16 ``[blocks][frames*tpf][heads][head_dim]``."""
+    shape = (blocks, frames * wl.tpf, wl.heads, wl.head_dim)
+    return tuple(_torch_normal(shape, _torch_seed(wl.seed, tag, segment, blocks), device, wl.outlier_p,
+                               wl.outlier_mag) for tag in (_TAG_HK, _TAG_HV))
