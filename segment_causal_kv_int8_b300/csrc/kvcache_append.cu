@@ -44,7 +44,7 @@ __device__ __forceinline__ void load8(const void* base, long long off, float (&x
   }
 }
 
-constexpr int kAppendTokens = 4;  // tokens per block (and rows per 16-lane group)
+constexpr int kAppendTokens = 2;  // tokens per block (and rows per 16-lane group)
 
 // Grid: x = groups of kAppendTokens tokens, y = groups of 16 heads, z = (block,
 // tensor).  16 lanes own one (token, head) row, 8 values each; the 16 row
@@ -52,8 +52,9 @@ constexpr int kAppendTokens = 4;  // tokens per block (and rows per 16-lane grou
 // ([heads][128] contiguous in the input) and writes, per head, kAppendTokens
 // consecutive ring slots.  Each lane group issues all its loads before any
 // arithmetic.
+// Many small CTAs (eight per SM for bf16 input) keep enough rows in flight.
 template <bool kF32In, bool kInt8>
-__global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
+__global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __grid_constant__ AppendParams p) {
   const int h = blockIdx.y * 16 + (threadIdx.x >> 4);
   if (h >= p.heads) return;  // whole 16-lane groups leave together
   const int g = threadIdx.x & 15;
