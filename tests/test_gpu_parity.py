@@ -236,3 +236,64 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert nomas.nomas_selftest_wait_timeout(0, nomas._stream_ptr()) == nomas.NOMAS_ERR_INVALID_ARG
     x = torch.arange(16, device="cuda", dtype=torch.float32)
     assert float(x.sum()) == 120.0
+
+
+def _poison(dtype):
+    return {torch.int8: -77, torch.uint8: 165}.get(dtype, -12288.0)  # exact in bf16 and fp32
+
+
+def _guarded(shape, dtype, guard=4096):
+    """A tensor viewed out of the middle of a larger one whose ends hold a poison pattern."""
+    n = int(np.prod(shape))
+    big = torch.empty(n + 2 * guard, dtype=dtype, device="cuda")
+    big.fill_(_poison(dtype))
+    return big, big[guard:guard + n].view(*shape), guard
+
+
+def _guards_intact(big, guard, dtype):
+    ends = torch.cat([big[:guard], big[-guard:]]).float()
+    return bool((ends == float(_poison(dtype))).all())
+
+
+@pytest.mark.parametrize("case", [0, 1, 2])
+def test_no_writes_outside_caller_buffers(case):
+    # Ragged shapes (tile tails on both key ranges and on the query side), INT8
+    # and BF16 caches, split and unsplit: poison guards around every buffer a
+    # kernel writes must survive append, RoPE and attention.
+    wl = small_variant(CONFIGS["c2_bf16_hist8"], **RAGGED[case], seed=300 + case)
+    hist = [segment_kv(wl, s, f, 0) for s, f in enumerate(wl.cache_frames_hist)]
+    slots = wl.capacity_frames * wl.tpf
+    kdt = torch.int8 if wl.cache_dtype == "int8" else torch.bfloat16
+    kb, kc, g = _guarded((1, wl.heads, slots, 128), kdt)
+    vb, vc, _ = _guarded((1, wl.heads, slots, 128), kdt)
+    gc = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames, wl.cache_dtype)
+    gc.k, gc.v = kc, vc
+    gc.desc.k, gc.desc.v = kc.data_ptr(), vc.data_ptr()
+    if wl.cache_dtype == "int8":
+        ksb, ksc, _ = _guarded((1, wl.heads, slots), torch.float32)
+        vsb, vsc, _ = _guarded((1, wl.heads, slots), torch.float32)
+        gc.k_scale, gc.v_scale = ksc, vsc
+        gc.desc.k_scale, gc.desc.v_scale = ksc.data_ptr(), vsc.data_ptr()
+    for k, v in hist:
+        gc.append(to_dev(k, "bf16"), to_dev(v, "bf16"))
+    q, k, v = current_qkv(wl)
+    qb, qd, _ = _guarded(q.shape, torch.bfloat16)
+    kcb, kd, _ = _guarded(k.shape, torch.bfloat16)
+    qd.copy_(to_dev(q, "bf16"))
+    kd.copy_(to_dev(k, "bf16"))
+    vd = to_dev(v, "bf16")
+    nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+    for splits in (1, 3):
+        ob, od, _ = _guarded(q.shape, torch.bfloat16)
+        lb, ld, _ = _guarded((wl.heads, wl.n_q), torch.float32)
+        nbytes = gc.workspace_bytes(wl.n_video, wl.n_text, splits)
+        wb, wd, _ = _guarded((max(nbytes, 256),), torch.uint8)
+        nomas.segment_attn(gc, 0, qd, kd, vd, wl.n_video, wl.n_text, out=od, lse=ld, workspace=wd,
+                           num_splits=splits)
+        torch.cuda.synchronize()
+        for big, dt in ((ob, torch.bfloat16), (lb, torch.float32), (wb, torch.uint8)):
+            assert _guards_intact(big, g, dt)
+    for big, dt in ((kb, kdt), (vb, kdt), (qb, torch.bfloat16), (kcb, torch.bfloat16)):
+        assert _guards_intact(big, g, dt)
+    if wl.cache_dtype == "int8":
+        assert _guards_intact(ksb, g, torch.float32) and _guards_intact(vsb, g, torch.float32)
