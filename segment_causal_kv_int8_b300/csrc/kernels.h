@@ -42,9 +42,11 @@ struct AppendParams {
   void* cv;
   float* ks;                     // scales (int8 only)
   float* vs;
+  int chunk_tokens;              // staged kernel: tokens per bulk-loaded chunk
+  uint32_t* err;                 // device error word (staged kernel's bounded waits)
 };
 
-cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, int sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------ reset
 cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);

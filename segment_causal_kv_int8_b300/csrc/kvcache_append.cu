@@ -15,13 +15,17 @@
 //
 // Codec bits (identical to the reference definition): scale = fl32(m / 127),
 // inv = fl32(127 / m) (IEEE round-to-nearest divisions), code =
-// clamp(cvt.rni(fl32(x * inv)), -127, 127); the float->int conversion maps NaN
-// (0 * inf on an all-zero row) to 0 and saturates +-inf.
+// rint(fl32(x * inv)) (ties to even), which lies in [-127, 127].  The rounding
+// adds 1.5 * 2^23 to the product and takes the code's byte from the sum's
+// bits.  When inv overflows (absmax below 127 / FLT_MAX) the products are
+// +-inf or NaN (0 * inf): that row takes a float->int conversion instead,
+// with NaN -> 0 and +-inf clamped to +-127.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace nomas {
 namespace {
@@ -41,6 +45,61 @@ __device__ __forceinline__ void load8(const void* base, long long off, float (&x
       x[2 * e] = __uint_as_float(u[e] << 16);
       x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
     }
+  }
+}
+
+// Quantise (or copy) one row from 8 values per lane of a 16-lane group and
+// write it to its ring slot.
+template <bool kInt8>
+__device__ __forceinline__ void write_row(const AppendParams& p, int tensor, long long dst_row, const float (&x)[8],
+                                          int g, unsigned gmask) {
+  if constexpr (kInt8) {
+    float m = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
+    const float scale = __fdiv_rn(m, 127.0f);
+    const float inv = __fdiv_rn(127.0f, m);
+    uint32_t lo, hi;
+    if (inv <= 3.0e38f) {
+      // |fl32(x * inv)| <= 127: adding 1.5 * 2^23 rounds it to an integer
+      // (nearest, ties to even) held in the low mantissa bits, whose low byte
+      // is the two's-complement code.
+      uint32_t b[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) b[e] = __float_as_uint(__fadd_rn(__fmul_rn(x[e], inv), 12582912.0f));
+      lo = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+      hi = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+    } else {
+      // inv overflowed (absmax below 127 / FLT_MAX): +-inf products clamp to
+      // +-127 and NaN (0 * inf) converts to 0.
+      lo = hi = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int c = __float2int_rn(__fmul_rn(x[e], inv));
+        c = max(-127, min(127, c));
+        const uint32_t byte = static_cast<uint32_t>(c) & 0xFFu;
+        if (e < 4)
+          lo |= byte << (8 * e);
+        else
+          hi |= byte << (8 * (e - 4));
+      }
+    }
+
+    int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+    if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
+  } else {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
+    uint4 w;
+    uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 t = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+      u[e] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+    *reinterpret_cast<uint4*>(dst) = w;
   }
 }
 
@@ -81,38 +140,115 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
-    if constexpr (kInt8) {
-      float m = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[r][e]));
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
-      const float scale = __fdiv_rn(m, 127.0f);
-      const float inv = __fdiv_rn(127.0f, m);
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        int c = __float2int_rn(__fmul_rn(x[r][e], inv));
-        c = max(-127, min(127, c));
-        const uint32_t byte = static_cast<uint32_t>(c) & 0xFFu;
-        if (e < 4)
-          lo |= byte << (8 * e);
-        else
-          hi |= byte << (8 * (e - 4));
+    write_row<kInt8>(p, tensor, dst_row, x[r], g, gmask);
+  }
+}
+
+// Staged append: persistent CTAs stream the input through shared memory.
+// The input of one (block, tensor) is [tokens][heads][128] with whole token
+// rows contiguous, so a chunk of chunk_tokens tokens is one contiguous range;
+// warp 8 bulk-loads chunks (copy engine) into a kStages-deep ring, warps 0-7
+// (16 groups of 16 lanes, one row per group at a time) convert them from
+// shared memory and write codes and scales.  Chunks go round-robin to CTAs.
+constexpr int kStages = 3;
+constexpr int kStagedThreads = 288;      // 8 consumer warps + 1 producer warp
+constexpr int kStageBytes = 32 * 1024;   // largest chunk
+
+template <bool kF32In, bool kInt8>
+__global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const __grid_constant__ AppendParams p) {
+  extern __shared__ __align__(128) uint8_t stage_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ AbortState ab;
+  constexpr int esz = kF32In ? 4 : 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row_elems = static_cast<long long>(p.heads) * 128;
+  const int T = p.chunk_tokens;
+  const int per = (p.n_tokens + T - 1) / T;          // chunks per (block, tensor)
+  const long long n_chunks = 2LL * p.blocks * per;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 8);  // one arrival per consumer warp
+    }
+    ab.flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (warp == 8) {
+    if (lane == 0) {
+      int i = 0;
+      bool ok = true;
+      for (long long q = blockIdx.x; q < n_chunks && ok; q += gridDim.x, ++i) {
+        const int s = i % kStages, u = i / kStages;
+        if (u > 0 && !lane_wait(&empty[s], (u - 1) & 1, &ab, p.err)) {
+          ok = false;
+          break;
+        }
+        const long long bt = q / per;
+        const int ci = static_cast<int>(q - bt * per);
+        const int b = static_cast<int>(bt >> 1), tensor = static_cast<int>(bt & 1);
+        const int n0 = ci * T, nt = min(T, p.n_tokens - n0);
+        const char* src = static_cast<const char*>(tensor ? p.v : p.k) +
+                          (b * p.block_stride + (static_cast<long long>(p.first_frame) * p.tpf + n0) * row_elems) * esz;
+        const uint32_t bytes = static_cast<uint32_t>(nt * row_elems * esz);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(stage_raw + s * kStageBytes, src, bytes, &full[s]);
       }
-      int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
-      *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-      if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
-    } else {
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 8 * g;
-      uint4 w;
-      uint32_t* u = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 t = __floats2bfloat162_rn(x[r][2 * e], x[r][2 * e + 1]);
-        u[e] = *reinterpret_cast<const uint32_t*>(&t);
+      if (!ok) {
+        // Abort: give the loads already issued time to land.
+        for (int j = i - 1; j >= 0 && j >= i - kStages; --j)
+          lane_wait_teardown(&full[j % kStages], (j / kStages) & 1, 20000000ull);
       }
-      *reinterpret_cast<uint4*>(dst) = w;
+    }
+  } else {
+    const int grp = threadIdx.x >> 4;  // 0..15
+    const int g = threadIdx.x & 15;
+    const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
+    int i = 0;
+    bool ok = true;
+    for (long long q = blockIdx.x; q < n_chunks && ok; q += gridDim.x, ++i) {
+      const int s = i % kStages, u = i / kStages;
+      if (!warp_wait(&full[s], u & 1, &ab, p.err)) {
+        ok = false;
+        break;
+      }
+      const long long bt = q / per;
+      const int ci = static_cast<int>(q - bt * per);
+      const int b = static_cast<int>(bt >> 1), tensor = static_cast<int>(bt & 1);
+      const int n0 = ci * T, nt = min(T, p.n_tokens - n0);
+      const int rows = nt * p.heads;
+      const uint8_t* stage = stage_raw + s * kStageBytes;
+      // Both 16-lane groups of a warp take the same number of rows.
+      for (int r = grp; r < ((rows + 15) & ~15); r += 16) {
+        if (r < rows) {
+          const int tok = r / p.heads, h = r - tok * p.heads;
+          float x[8];
+          const uint8_t* src = stage + ((static_cast<long long>(tok) * p.heads + h) * 128 + 8 * g) * esz;
+          if constexpr (kF32In) {
+            const float4 a = *reinterpret_cast<const float4*>(src);
+            const float4 c = *reinterpret_cast<const float4*>(src + 16);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+          } else {
+            const uint4 w = *reinterpret_cast<const uint4*>(src);
+            const uint32_t uu[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              x[2 * e] = __uint_as_float(uu[e] << 16);
+              x[2 * e + 1] = __uint_as_float(uu[e] & 0xFFFF0000u);
+            }
+          }
+          const int n = n0 + tok;
+          const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+          int slot_frame = p.base_slot_frame + f;
+          if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
+          const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
+                                    static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
+          write_row<kInt8>(p, tensor, dst_row, x, g, gmask);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
 }
@@ -128,8 +264,34 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint8_t* __restrict__ pt
 
 }  // namespace
 
-cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, cudaStream_t stream) {
-  if (p.n_tokens <= 0 || p.blocks <= 0 || p.heads <= 0) return cudaSuccess;
+cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p_in, int sms, cudaStream_t stream) {
+  if (p_in.n_tokens <= 0 || p_in.blocks <= 0 || p_in.heads <= 0) return cudaSuccess;
+  AppendParams p = p_in;
+  const long long token_bytes = static_cast<long long>(p.heads) * 128 * (f32_in ? 4 : 2);
+  const long long in_bytes = 2LL * p.blocks * p.n_tokens * token_bytes;
+  // Large appends (a whole session's worth of blocks) stream through shared
+  // memory; small ones finish sooner with the direct kernel's many small CTAs.
+  if (sms > 0 && p.err != nullptr && token_bytes <= kStageBytes && in_bytes >= (256LL << 20)) {
+    // Staged path: chunks of up to 32 KB of whole token rows.
+    p.chunk_tokens = static_cast<int>(kStageBytes / token_bytes);
+    const long long chunks = 2LL * p.blocks * ((p.n_tokens + p.chunk_tokens - 1) / p.chunk_tokens);
+    const unsigned grid = static_cast<unsigned>(chunks < 2LL * sms ? chunks : 2LL * sms);
+    static int configured[64][4] = {{0}};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int idx = (f32_in ? 2 : 0) + (int8_cache ? 1 : 0);
+    const size_t smem = kStages * kStageBytes;
+    auto kern = f32_in ? (int8_cache ? append_staged_kernel<true, true> : append_staged_kernel<true, false>)
+                       : (int8_cache ? append_staged_kernel<false, true> : append_staged_kernel<false, false>);
+    if (dev >= 0 && dev < 64 && !configured[dev][idx]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      configured[dev][idx] = 1;
+    }
+    kern<<<grid, kStagedThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
                   static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
   if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;

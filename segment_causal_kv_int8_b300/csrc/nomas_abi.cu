@@ -287,7 +287,14 @@ NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k,
     p.cv = cache->v;
     p.ks = cache->k_scale;
     p.vs = cache->v_scale;
-    st = from_cuda(launch_append(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, stream));
+    p.chunk_tokens = 0;
+    p.err = nullptr;
+    int sms = 0;
+    if (device_state(&p.err, &sms) != NOMAS_OK) {
+      p.err = nullptr;
+      sms = 0;
+    }
+    st = from_cuda(launch_append(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, sms, stream));
     if (st != NOMAS_OK) return st;
   }
   cache->total_frames = new_total;
