@@ -144,6 +144,102 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
   }
 }
 
+// Direct append for bf16 input: 8 lanes own a row (16 values each, two
+// 16-byte loads), so the per-row reduction and the two divisions are shared by
+// twice as many values.  Grid: x = groups of kAppendTokens tokens, y = groups
+// of 32 heads, z = (block, tensor); a CTA's 32 row groups are consecutive
+// heads.  A BF16 cache takes the bf16 values unchanged (a copy).
+template <bool kInt8>
+__global__ void __launch_bounds__(256, kInt8 ? 6 : 8) append8_kernel(const __grid_constant__ AppendParams p) {
+  const int h = blockIdx.y * 32 + (threadIdx.x >> 3);
+  if (h >= p.heads) return;  // whole 8-lane groups leave together
+  const int g = threadIdx.x & 7;
+  const unsigned gmask = 0xFFu << (threadIdx.x & 24);
+  const int tensor = blockIdx.z & 1;
+  const int b = blockIdx.z >> 1;
+  const int n0 = blockIdx.x * kAppendTokens;
+  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(tensor ? p.v : p.k);
+  const long long plane = static_cast<long long>(b) * p.heads + h;
+  uint4 w[kAppendTokens][2];
+#pragma unroll
+  for (int r = 0; r < kAppendTokens; ++r) {
+    const int n = n0 + r;
+    if (n < p.n_tokens) {
+      const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
+      const uint4* q = reinterpret_cast<const uint4*>(src + b * p.block_stride + (src_tok * p.heads + h) * 128 + 16 * g);
+      w[r][0] = q[0];
+      w[r][1] = q[1];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kAppendTokens; ++r) {
+    const int n = n0 + r;
+    if (n >= p.n_tokens) break;
+    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    int slot_frame = p.base_slot_frame + f;
+    if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
+    const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
+    if constexpr (kInt8) {
+      const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
+      float x[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[2 * e] = __uint_as_float(u[e] << 16);
+        x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+      }
+      float m0 = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      float m1 = fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7])));
+      float m2 = fmaxf(fmaxf(fabsf(x[8]), fabsf(x[9])), fmaxf(fabsf(x[10]), fabsf(x[11])));
+      float m3 = fmaxf(fmaxf(fabsf(x[12]), fabsf(x[13])), fmaxf(fabsf(x[14]), fabsf(x[15])));
+      float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+      for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
+      const float scale = __fdiv_rn(m, 127.0f);
+      const float inv = __fdiv_rn(127.0f, m);
+      uint32_t c[4];
+      if (inv <= 3.0e38f) {
+        // rint(fl32(x * inv)) in [-127, 127]: adding 1.5 * 2^23 rounds to an
+        // integer (ties to even) whose low byte is the two's-complement code.
+        // The product is rounded on its own (the packed multiply) and the add
+        // is a separate scalar __fadd_rn, so nothing fuses the two into an FMA.
+        const uint64_t inv2 = f2_pack(inv, inv);
+        uint32_t bb[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float y0, y1;
+          f2_unpack(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), y0, y1);
+          bb[2 * e] = __float_as_uint(__fadd_rn(y0, 12582912.0f));
+          bb[2 * e + 1] = __float_as_uint(__fadd_rn(y1, 12582912.0f));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          c[q] = __byte_perm(__byte_perm(bb[4 * q], bb[4 * q + 1], 0x0040), __byte_perm(bb[4 * q + 2], bb[4 * q + 3], 0x0040),
+                             0x5410);
+      } else {
+        // inv overflowed (absmax below 127 / FLT_MAX): +-inf products clamp to
+        // +-127 and NaN (0 * inf) converts to 0.
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          c[q] = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            int ci = __float2int_rn(__fmul_rn(x[4 * q + e], inv));
+            ci = max(-127, min(127, ci));
+            c[q] |= (static_cast<uint32_t>(ci) & 0xFFu) << (8 * e);
+          }
+        }
+      }
+      int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
+      if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g);
+      dst[0] = w[r][0];
+      dst[1] = w[r][1];
+    }
+  }
+}
+
 // Staged append: persistent CTAs stream the input through shared memory.
 // The input of one (block, tensor) is [tokens][heads][128] with whole token
 // rows contiguous, so a chunk of chunk_tokens tokens is one contiguous range;
@@ -290,6 +386,16 @@ cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p_in
       configured[dev][idx] = 1;
     }
     kern<<<grid, kStagedThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  if (!f32_in) {
+    const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
+                    static_cast<unsigned>((p.heads + 31) / 32), static_cast<unsigned>(2 * p.blocks));
+    if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+    if (int8_cache)
+      append8_kernel<true><<<grid, 256, 0, stream>>>(p);
+    else
+      append8_kernel<false><<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
   }
   const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
