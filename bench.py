@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
+    ap.add_argument("--archive", action="store_true",
+                    help="session workload: also copy every appended frame to a host archive")
     return ap.parse_args()
 
 
@@ -535,9 +537,14 @@ def run_session(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     calls = [0]
+    archive = None
+    if args.archive:
+        # Host KV archive of every appended frame (pinned, one session's worth).
+        archive = torch.empty(turns * wl.cur_frames * cache.archive_frame_bytes(), dtype=torch.uint8).pin_memory()
 
     def session():
         cache.reset(zero_memory=False)
+        used = 0
         for t in range(turns):
             for s in range(wl.steps):
                 for blk in range(wl.blocks):
@@ -546,7 +553,10 @@ def run_session(args):
                                  wl.rope_split)
                     nomas.segment_attn(cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
                     calls[0] += 2
-            cache.append(seg_k, seg_v)
+            if archive is not None:
+                used = cache.append_archive(seg_k, seg_v, archive, used)
+            else:
+                cache.append(seg_k, seg_v)
             calls[0] += 1
 
     for _ in range(args.warmup):
@@ -581,6 +591,7 @@ def run_session(args):
                                    f"segment attention ({wl.heads} heads x {wl.head_dim}, Nq={wl.n_q}, INT8 cache "
                                    f"window {wl.window} frames), one 54-block append per turn; one step = one session",
                        "turns": turns, "attention_calls": turns * wl.steps * wl.blocks,
+                       "host_archive": bool(args.archive),
                        "l2": "working set (54 blocks' caches, input pool) far larger than L2",
                        "parallelism": f"replica x{world} (independent sessions per GPU)"},
             "roofline": {"bound": "tensor", "achieved": value / world, "peak": float(peaks["bf16_tflops_sustained"]),

@@ -161,6 +161,38 @@ nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k, const voi
                                   int64_t block_stride_elems, cudaStream_t stream);
 
 /*
+ * Host archive of every appended frame (the CPU KV archive of the low-memory
+ * recipe: the GPU keeps the last past_frames latent frames, all earlier ones
+ * live in host RAM; "System-RAM" on the inferencekey.com RTX 4090 test page
+ * logs cpu_archive_gib growing by about 5.88 GiB per 30-frame segment).
+ *
+ * nomas_kvcache_archive_frame_bytes: host bytes one archived frame takes,
+ * 2 * blocks * heads * grid_h * grid_w * (head_dim + 4); 0 for an invalid or
+ * non-INT8 descriptor.  Host only.
+ *
+ * nomas_kvcache_append_archive: nomas_kvcache_append of an INT8 cache that
+ * also copies every frame of the segment, once quantised, to host memory at
+ * archive + *archive_used, in increasing frame order, and advances
+ * *archive_used.  One archived frame is: K codes, V codes
+ * ([blocks][heads][grid_h*grid_w][head_dim] int8 each), then K scales, V
+ * scales ([blocks][heads][grid_h*grid_w] float32 each).  The segment is
+ * appended in chunks of at most one window, so frames that fall out of the
+ * window within the segment are still archived; the cache ends in the same
+ * state as after nomas_kvcache_append.  The copies are asynchronous on
+ * `stream` (pinned host memory makes them overlap other work); read the
+ * archive after synchronising the stream.
+ *
+ *   archive, archive_bytes  caller-owned host buffer and its size
+ *   archive_used            in/out: bytes already used
+ * Returns NOMAS_ERR_UNSUPPORTED for a BF16 cache, NOMAS_ERR_CAPACITY (nothing
+ * enqueued) when the archive or a cache without a window would overflow.
+ */
+size_t nomas_kvcache_archive_frame_bytes(const nomas_kvcache* cache);
+nomas_status nomas_kvcache_append_archive(nomas_kvcache* cache, const void* k, const void* v, nomas_dtype in_dt,
+                                          int32_t n_frames, int64_t block_stride_elems, void* archive,
+                                          size_t archive_bytes, size_t* archive_used, cudaStream_t stream);
+
+/*
  * Scratch bytes nomas_segment_attn needs for a given split count (0 = the
  * split count it would choose itself).  Host only.
  */

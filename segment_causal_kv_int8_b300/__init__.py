@@ -77,6 +77,9 @@ EXPORTS = {
     "nomas_rope3d_apply": (_c_int, [_vp, _vp, _c_int, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i64, _f32,
                                     _i32, _i32, _i32, _vp]),
     "nomas_kvcache_append": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _vp]),
+    "nomas_kvcache_archive_frame_bytes": (_sz, [_P(nomas_kvcache)]),
+    "nomas_kvcache_append_archive": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _vp, _sz, _P(_sz),
+                                              _vp]),
     "nomas_segment_attn_workspace_bytes": (_c_int, [_P(nomas_kvcache), _i32, _i32, _i32, _P(_sz)]),
     "nomas_segment_attn": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
                                     _sz, _i32, _vp]),
@@ -211,6 +214,28 @@ class KVCache:
         _check(nomas_kvcache_append(ctypes.byref(self.desc), ctypes.c_void_p(k.data_ptr()),
                                     ctypes.c_void_p(v.data_ptr()), _dt_code(k), k.shape[1] // self.tpf,
                                     k.stride(0), _stream_ptr(stream)), "nomas_kvcache_append")
+
+    def archive_frame_bytes(self) -> int:
+        return int(nomas_kvcache_archive_frame_bytes(ctypes.byref(self.desc)))
+
+    def append_archive(self, k, v, archive, used: int = 0, stream=None) -> int:
+        """Append like :meth:`append` (INT8 cache) and copy every frame of the segment to ``archive``
+        (a host uint8 tensor, pinned for asynchronous copies) from byte ``used`` on; returns the new
+        byte count.  Synchronise the stream before reading the archive."""
+        if k.dim() == 3:
+            k, v = k.unsqueeze(0), v.unsqueeze(0)
+        if k.shape != v.shape or k.dtype != v.dtype or not k.is_cuda:
+            raise ValueError("k and v must be CUDA tensors of equal shape and dtype")
+        if k.shape[0] != self.desc.num_blocks or k.shape[2] != self.desc.heads or k.shape[1] % self.tpf:
+            raise ValueError("K/V shape does not match the cache")
+        if archive.is_cuda or archive.dtype.itemsize != 1 or not archive.is_contiguous():
+            raise ValueError("archive must be a contiguous host byte tensor")
+        n = ctypes.c_size_t(used)
+        _check(nomas_kvcache_append_archive(ctypes.byref(self.desc), ctypes.c_void_p(k.data_ptr()),
+                                            ctypes.c_void_p(v.data_ptr()), _dt_code(k), k.shape[1] // self.tpf,
+                                            k.stride(0), ctypes.c_void_p(archive.data_ptr()), archive.numel(),
+                                            ctypes.byref(n), _stream_ptr(stream)), "nomas_kvcache_append_archive")
+        return int(n.value)
 
     def reset(self, zero_memory: bool = False, stream=None) -> None:
         _check(nomas_kvcache_reset(ctypes.byref(self.desc), int(bool(zero_memory)), _stream_ptr(stream)),

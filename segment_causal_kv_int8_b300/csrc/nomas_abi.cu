@@ -302,6 +302,69 @@ NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k,
   return NOMAS_OK;
 }
 
+NOMAS_API size_t nomas_kvcache_archive_frame_bytes(const nomas_kvcache* c) {
+  if (validate_cache(c) != NOMAS_OK || c->dtype != NOMAS_INT8) return 0;
+  const size_t rows = static_cast<size_t>(c->num_blocks) * c->heads * c->grid_h * c->grid_w;
+  return 2 * rows * (static_cast<size_t>(c->head_dim) + 4);
+}
+
+NOMAS_API nomas_status nomas_kvcache_append_archive(nomas_kvcache* cache, const void* k, const void* v,
+                                                    nomas_dtype in_dt, int32_t n_frames, int64_t block_stride_elems,
+                                                    void* archive, size_t archive_bytes, size_t* archive_used,
+                                                    cudaStream_t stream) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (cache->dtype != NOMAS_INT8) return NOMAS_ERR_UNSUPPORTED;
+  if (archive == nullptr || archive_used == nullptr || n_frames < 0) return NOMAS_ERR_INVALID_ARG;
+  if (in_dt != NOMAS_F32 && in_dt != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
+  st = plan(cache, n_frames, nullptr, nullptr, nullptr, nullptr);
+  if (st != NOMAS_OK) return st;
+  const size_t frame_bytes = nomas_kvcache_archive_frame_bytes(cache);
+  if (*archive_used > archive_bytes || static_cast<size_t>(n_frames) * frame_bytes > archive_bytes - *archive_used)
+    return NOMAS_ERR_CAPACITY;
+  const int64_t tpf = static_cast<int64_t>(cache->grid_h) * cache->grid_w;
+  const int64_t planes = static_cast<int64_t>(cache->num_blocks) * cache->heads;
+  const int64_t cap_slots = tpf * cache->capacity_frames;
+  const int64_t esz = in_dt == NOMAS_F32 ? 4 : 2;
+  const int64_t frame_elems = tpf * cache->heads * cache->head_dim;  // per block of the input
+  const int64_t window = window_of(cache);
+  const size_t code_bytes = static_cast<size_t>(planes * tpf * cache->head_dim);
+  const size_t scale_bytes = static_cast<size_t>(planes * tpf * 4);
+  uint8_t* dst = static_cast<uint8_t*>(archive) + *archive_used;
+  // Chunks of at most one window: every frame of the segment passes through
+  // the ring (so it is quantised there) and is copied out before a later
+  // chunk of the same segment could overwrite its slot.
+  for (int32_t done = 0; done < n_frames;) {
+    const int32_t chunk = static_cast<int32_t>(std::min<int64_t>(window, n_frames - done));
+    const char* kc = static_cast<const char*>(k) + static_cast<int64_t>(done) * frame_elems * esz;
+    const char* vc = static_cast<const char*>(v) + static_cast<int64_t>(done) * frame_elems * esz;
+    st = nomas_kvcache_append(cache, kc, vc, in_dt, chunk, block_stride_elems, stream);
+    if (st != NOMAS_OK) return st;
+    for (int32_t i = 0; i < chunk; ++i) {
+      const int64_t slot = (cache->total_frames - chunk + i) % cache->capacity_frames;
+      // Per frame: K codes, V codes [planes][tpf][head_dim], then K scales, V
+      // scales [planes][tpf]; each a strided 2-D copy out of the ring.
+      const void* src[4] = {static_cast<const int8_t*>(cache->k) + slot * tpf * cache->head_dim,
+                            static_cast<const int8_t*>(cache->v) + slot * tpf * cache->head_dim,
+                            cache->k_scale + slot * tpf, cache->v_scale + slot * tpf};
+      const size_t width[4] = {static_cast<size_t>(tpf * cache->head_dim), static_cast<size_t>(tpf * cache->head_dim),
+                               static_cast<size_t>(tpf * 4), static_cast<size_t>(tpf * 4)};
+      const size_t pitch[4] = {static_cast<size_t>(cap_slots * cache->head_dim),
+                               static_cast<size_t>(cap_slots * cache->head_dim), static_cast<size_t>(cap_slots * 4),
+                               static_cast<size_t>(cap_slots * 4)};
+      for (int j = 0; j < 4; ++j) {
+        if (cudaMemcpy2DAsync(dst, width[j], src[j], pitch[j], width[j], static_cast<size_t>(planes),
+                              cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+          return NOMAS_ERR_CUDA;
+        dst += j < 2 ? code_bytes : scale_bytes;
+      }
+      *archive_used += frame_bytes;
+    }
+    done += chunk;
+  }
+  return NOMAS_OK;
+}
+
 NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;

@@ -137,3 +137,18 @@ def test_workspace_bytes_for_explicit_splits():
     nq = 7616
     want = -(-4 * 16 * nq * 128 * 4 // 256) * 256 + -(-4 * 16 * nq * 4 // 256) * 256
     assert out.value == want
+
+
+def test_archive_frame_bytes_matches_the_archive_growth_on_the_page():
+    # One archived frame holds INT8 K and V codes plus a float32 scale per
+    # (block, head, token); 30 frames of a segment at 54 x 16 x 128 on a 23x40
+    # grid come within 0.5% of the growth the page logs per segment.
+    d = _desc(blocks=54, heads=16, gh=23, gw=40, cap=18)
+    d.past_frames = 18
+    fb = nomas.nomas_kvcache_archive_frame_bytes(ctypes.byref(d))
+    assert fb == 2 * 54 * 16 * 23 * 40 * (128 + 4)
+    for gib_logged, segments in ((5.881, 1), (11.763, 2), (17.644, 3)):
+        assert abs(segments * 30 * fb / 2 ** 30 / gib_logged - 1) < 0.005
+    d16 = _desc(blocks=54, heads=16, gh=23, gw=40, cap=18, dtype=nomas.NOMAS_BF16)
+    d16.past_frames = 18
+    assert nomas.nomas_kvcache_archive_frame_bytes(ctypes.byref(d16)) == 0
