@@ -15,6 +15,8 @@ int8_codec   per-(token, head) absmax INT8 quantisation of K/V rows
 ring_cache   the persistent, optionally windowed ring of latent frames
 attention    segment attention over [resident cache ; current segment] and the
              equivalent full-sequence masked formulation
+sparse       block-sparse variant: per query group, the highest-scoring cache
+             key tiles plus all current keys
 
 Parity status: every function here is pinned by the ``tests/test_oracle_*``
 suite (closed forms, invariants, brute force and the pages' printed numbers),
@@ -22,6 +24,6 @@ except the RoPE pairing convention and the text-token positions, which the
 pages leave open; those two readings are "parity unpinned" beyond the oracle's
 own definition (see rope3d's docstring).
 """
-from . import attention, int8_codec, ring_cache, rope3d
+from . import attention, int8_codec, ring_cache, rope3d, sparse
 
-__all__ = ["attention", "int8_codec", "ring_cache", "rope3d"]
+__all__ = ["attention", "int8_codec", "ring_cache", "rope3d", "sparse"]
