@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
+    ap.add_argument("--sparse", type=float, default=0.0,
+                    help="block-sparse attention keeping this fraction of cache tiles (0 = dense)")
     ap.add_argument("--archive", action="store_true",
                     help="session workload: also copy every appended frame to a host archive")
     return ap.parse_args()
@@ -262,6 +264,20 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
+    keep = args.sparse
+    if keep:
+        import ctypes
+        n_tiles = (wl.n_cache + 127) // 128
+        groups = (wl.n_q + 511) // 512
+        sel_tiles = torch.zeros((wl.heads, groups, max(1, nomas.sparse_keep_count(n_tiles, keep))),
+                                dtype=torch.int32, device=dev)
+        sel_counts = torch.zeros((wl.heads, groups), dtype=torch.int32, device=dev)
+        b = ctypes.c_size_t()
+        d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
+        d.total_frames = sum(wl.cache_frames_hist)
+        d.valid_frames = min(d.total_frames, wl.window)
+        nomas.nomas_sparse_select_workspace_bytes(ctypes.byref(d), wl.n_video, wl.n_text, ctypes.byref(b))
+        sel_ws = torch.empty(max(256, b.value), dtype=torch.uint8, device=dev)
 
     def evict_l2():
         # Write a buffer twice the L2 size, then read it back: the inputs leave
@@ -271,7 +287,7 @@ def run_ours(args):
         flush.view(torch.int32).sum()
 
     def step(ev=None):
-        # ev: None or 6 events bracketing append, RoPE and attention
+        # ev: None or 8 events bracketing append, RoPE, attention and (sparse) tile selection
         cache.reset(zero_memory=False)
         if ev is not None:
             ev[0].record(stream)
@@ -283,9 +299,21 @@ def run_ours(args):
         nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
         if ev is not None:
             ev[3].record(stream)
+        if keep:
+            if ev is not None:
+                ev[6].record(stream)
+            nomas.sparse_select(cache, 0, q, wl.n_video, wl.n_text, keep, tiles=sel_tiles, counts=sel_counts,
+                                workspace=sel_ws)
+            if ev is not None:
+                ev[7].record(stream)
+        if ev is not None:
             ev[4].record(stream)
-        nomas.segment_attn(cache, 0, q, k, v, wl.n_video, wl.n_text, out=out, lse=lse, workspace=ws,
-                           num_splits=args.num_splits)
+        if keep:
+            nomas.segment_attn_sparse(cache, 0, q, k, v, wl.n_video, wl.n_text, sel_tiles, sel_counts, out=out,
+                                      lse=lse, workspace=ws, num_splits=args.num_splits)
+        else:
+            nomas.segment_attn(cache, 0, q, k, v, wl.n_video, wl.n_text, out=out, lse=lse, workspace=ws,
+                               num_splits=args.num_splits)
         if ev is not None:
             ev[5].record(stream)
 
@@ -299,7 +327,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(dev.index if world == 1 else local)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -322,6 +350,7 @@ def run_ours(args):
     append_ms = [e[2].elapsed_time(e[3]) for e in evs]
     rope_ms = [e[4].elapsed_time(e[5]) for e in evs]
     attn_ms = [e[6].elapsed_time(e[7]) for e in evs]
+    select_ms = [e[8].elapsed_time(e[9]) for e in evs] if keep else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -329,15 +358,17 @@ def run_ours(args):
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     flops = wl.attn_flops()
+    if keep:
+        flops = sparse_flops(wl, sel_tiles.cpu().numpy(), sel_counts.cpu().numpy())
     value = whole_job_value(flops, world, args.steps, total_ms)
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not keep:
         e2e = _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world)
 
-    launches_per_step = len(hist) + 1 + 1 + (1 if splits_used > 1 else 0)
+    launches_per_step = len(hist) + 1 + 1 + (1 if splits_used > 1 else 0) + (3 if keep and wl.n_cache else 0)
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -369,6 +400,16 @@ def run_ours(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if keep:
+            # Executed FLOPs count each query group's kept keys; the dense
+            # equivalent is the full-attention FLOPs over the same step time.
+            line["config"]["workload"] += f"; block-sparse, keep {keep} of the cache tiles"
+            line["sparse"] = {"keep": keep, "select_us": 1e3 * statistics.mean(select_ms),
+                              "executed_flops": flops, "dense_flops": wl.attn_flops(),
+                              "dense_equivalent_tflops": whole_job_value(wl.attn_flops(), world, args.steps,
+                                                                         total_ms)}
+            line["roofline"]["kernel"] += " (tile lists)"
+            line["roofline"]["traffic"] = None
         if not args.no_cpu_baseline and world == 1:
             v_cpu, desc, threads, _ = oracle_sample(wl, args.cpu_seconds)
             line["cpu_baseline"] = {"value": v_cpu / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -377,6 +418,17 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def sparse_flops(wl, tiles, counts) -> float:
+    """4 * D * sum over (head, query group) of rows x (kept cache keys + current keys)."""
+    total = 0.0
+    for h in range(wl.heads):
+        for g in range(counts.shape[1]):
+            rows = min(wl.n_q, 512 * (g + 1)) - 512 * g
+            kept = sum(min(128, wl.n_cache - 128 * int(t)) for t in tiles[h, g, :counts[h, g]])
+            total += 4.0 * wl.head_dim * rows * (kept + wl.n_q)
+    return total
 
 
 def _workspace_for(nomas, cache, wl, num_splits):

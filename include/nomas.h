@@ -225,6 +225,61 @@ nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const
                                 cudaStream_t stream);
 
 /*
+ * Block-sparse segment attention.  The single-GPU preset of the RTX 4090
+ * guide lists a sparse attention backend that, after two dense denoising
+ * steps, attends to a quarter of the candidate video key blocks (Hy-Nomas auf
+ * einer RTX 4090, section "Das Single-GPU-Preset").  The pages give no block
+ * size and no selection rule; this library reads them as follows.  A
+ * candidate is a key tile of 128 resident cache slots (tile t = slots
+ * [128 t, 128 t + 128) of the resident cache, the last one partial); the
+ * current segment's own keys are always attended.  Queries form groups of 512
+ * rows (g = row / 512).  For head h and group g, tile t scores
+ * mean_query(h, g) . mean_key(h, t) (INT8 keys dequantised), and the
+ * k = min(T, ceil(keep_fraction * T)) best tiles are kept (equal scores: the
+ * lower tile first), listed in increasing tile order.
+ *
+ * nomas_sparse_select_workspace_bytes: device scratch nomas_sparse_select
+ * needs (the mean keys and mean queries, float32).  Host only.
+ *
+ * nomas_sparse_select: compute the kept lists for one block.
+ *   q               device bf16 [n_video + n_text][heads][head_dim] (the
+ *                   queries that will attend, after RoPE)
+ *   keep_fraction   in (0, 1]; 0.25 in the preset
+ *   tiles           device int32 [heads][groups][max_keep]: row (h, g) gets
+ *                   its kept tiles in its first counts[h, g] entries; the rest
+ *                   of the row is left untouched
+ *   counts          device int32 [heads][groups], groups = ceil((n_video + n_text) / 512)
+ *   max_keep        row length of `tiles`; must be >= k
+ *   workspace       device scratch, 256-byte aligned, of at least the bytes
+ *                   nomas_sparse_select_workspace_bytes reports
+ * Returns NOMAS_ERR_INVALID_ARG (nothing enqueued) for a bad argument and
+ * NOMAS_ERR_UNSUPPORTED for more than 8192 resident tiles.  An empty cache
+ * gives counts of 0.
+ *
+ * nomas_segment_attn_sparse: nomas_segment_attn where the queries of group g,
+ * head h see only the cache tiles tiles[h, g, 0 .. counts[h, g]) plus every
+ * current key.  Arguments as nomas_segment_attn, plus tiles, counts and
+ * max_keep laid out as above (any increasing list of valid tiles, not only
+ * one from nomas_sparse_select; counts are clamped to [0, min(max_keep, T)]).
+ * A list entry outside [0, T) is clamped into the cache and records
+ * NOMAS_ERR_INVALID_ARG in the device error word.  The workspace
+ * nomas_segment_attn_workspace_bytes reports for the same split count
+ * suffices.  With every tile kept the result equals nomas_segment_attn's.
+ */
+nomas_status nomas_sparse_select_workspace_bytes(const nomas_kvcache* cache, int32_t n_video,
+                                                 int32_t n_text, size_t* bytes);
+nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t block, const void* q,
+                                 int32_t n_video, int32_t n_text, float keep_fraction,
+                                 int32_t* tiles, int32_t* counts, int32_t max_keep,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int32_t block, const void* q,
+                                       const void* k_cur, const void* v_cur, int32_t n_video,
+                                       int32_t n_text, float softmax_scale, const int32_t* tiles,
+                                       const int32_t* counts, int32_t max_keep, void* out,
+                                       float* lse, void* workspace, size_t workspace_bytes,
+                                       int32_t num_splits, cudaStream_t stream);
+
+/*
  * Scratch capacity, in bytes, of nomas_segment_attn_noalloc (one array per
  * device, held for the life of the process).
  */

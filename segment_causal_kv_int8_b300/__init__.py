@@ -85,6 +85,11 @@ EXPORTS = {
                                     _sz, _i32, _vp]),
     "nomas_segment_attn_noalloc": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
                                             _i32, _vp]),
+    "nomas_sparse_select_workspace_bytes": (_c_int, [_P(nomas_kvcache), _i32, _i32, _P(_sz)]),
+    "nomas_sparse_select": (_c_int, [_P(nomas_kvcache), _i32, _vp, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _sz,
+                                     _vp]),
+    "nomas_segment_attn_sparse": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
+                                           _i32, _vp, _vp, _vp, _sz, _i32, _vp]),
     "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
     "nomas_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _vp]),
     "nomas_device_error": (_c_int, [_P(_c_int), _c_int]),
@@ -277,6 +282,84 @@ def segment_attn(cache: KVCache, block: int, q, k_cur, v_cur, n_video: int, n_te
     return out
 
 
+def _check_lists(torch, tiles, counts, heads: int, groups: int) -> None:
+    if tiles.dtype != torch.int32 or counts.dtype != torch.int32 or not tiles.is_contiguous() \
+            or not counts.is_contiguous() or not tiles.is_cuda or not counts.is_cuda:
+        raise ValueError("tiles and counts must be contiguous int32 CUDA tensors")
+    if tiles.dim() != 3 or tuple(tiles.shape[:2]) != (heads, groups) or tiles.shape[2] < 1 \
+            or tuple(counts.shape) != (heads, groups):
+        raise ValueError(f"tiles must be [{heads}][{groups}][max_keep] and counts [{heads}][{groups}]")
+
+
+def sparse_keep_count(n_tiles: int, keep_fraction: float) -> int:
+    """Tiles kept per (head, query group) out of ``n_tiles`` resident cache tiles."""
+    return min(n_tiles, max(0, math.ceil(keep_fraction * n_tiles - 1e-9)))
+
+
+def sparse_select(cache: KVCache, block: int, q, n_video: int, n_text: int, keep_fraction: float = 0.25,
+                  tiles=None, counts=None, workspace=None, stream=None):
+    """Kept cache tiles of block-sparse attention; returns ``(tiles, counts)``.
+
+    ``tiles``: int32 ``[heads][groups][max_keep]`` (first ``counts[h, g]``
+    entries of a row valid, increasing), ``counts``: int32 ``[heads][groups]``,
+    groups = ceil((n_video + n_text) / 512).  Allocated when not given.
+    """
+    torch = _torch()
+    if not q.is_cuda or q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bfloat16 CUDA tensor")
+    nq = n_video + n_text
+    heads = cache.desc.heads
+    groups = (nq + 511) // 512
+    n_tiles = (cache.valid_frames * cache.tpf + 127) // 128
+    if tiles is None:
+        tiles = torch.zeros((heads, groups, max(1, sparse_keep_count(n_tiles, keep_fraction))),
+                            dtype=torch.int32, device=q.device)
+    if counts is None:
+        counts = torch.zeros((heads, groups), dtype=torch.int32, device=q.device)
+    _check_lists(torch, tiles, counts, heads, groups)
+    need = ctypes.c_size_t(0)
+    _check(nomas_sparse_select_workspace_bytes(ctypes.byref(cache.desc), n_video, n_text, ctypes.byref(need)),
+           "nomas_sparse_select_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(max(256, need.value), dtype=torch.uint8, device=q.device)
+    _check(nomas_sparse_select(ctypes.byref(cache.desc), block, ctypes.c_void_p(q.data_ptr()), n_video, n_text,
+                               keep_fraction, ctypes.c_void_p(tiles.data_ptr()), ctypes.c_void_p(counts.data_ptr()),
+                               tiles.shape[-1], ctypes.c_void_p(workspace.data_ptr()),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "nomas_sparse_select")
+    return tiles, counts
+
+
+def segment_attn_sparse(cache: KVCache, block: int, q, k_cur, v_cur, n_video: int, n_text: int, tiles, counts,
+                        softmax_scale: Optional[float] = None, out=None, lse=None, workspace=None,
+                        num_splits: int = 0, stream=None):
+    """Block-sparse segment attention over the kept tiles of :func:`sparse_select`; returns ``out``."""
+    torch = _torch()
+    for t in (q, k_cur, v_cur):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k_cur, v_cur must be contiguous bfloat16 CUDA tensors")
+    nq = n_video + n_text
+    if q.shape[0] != nq or q.shape != k_cur.shape or q.shape != v_cur.shape:
+        raise ValueError("q/k_cur/v_cur must be [n_video + n_text][heads][128]")
+    _check_lists(torch, tiles, counts, cache.desc.heads, (nq + 511) // 512)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[2])
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(nomas_segment_attn_sparse(ctypes.byref(cache.desc), block, ctypes.c_void_p(q.data_ptr()),
+                                     ctypes.c_void_p(k_cur.data_ptr()), ctypes.c_void_p(v_cur.data_ptr()), n_video,
+                                     n_text, softmax_scale, ctypes.c_void_p(tiles.data_ptr()),
+                                     ctypes.c_void_p(counts.data_ptr()), tiles.shape[-1],
+                                     ctypes.c_void_p(out.data_ptr()),
+                                     ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                                     ctypes.c_void_p(ws_ptr), ws_bytes, num_splits, _stream_ptr(stream)),
+           "nomas_segment_attn_sparse")
+    return out
+
+
 def device_error(clear: bool = True) -> int:
     """The device-side error word (0 = none), read synchronously."""
     st = ctypes.c_int(0)
@@ -284,5 +367,6 @@ def device_error(clear: bool = True) -> int:
     return int(st.value)
 
 
-__all__ = ["KVCache", "rope3d", "segment_attn", "device_error", "NomasError", "nomas_kvcache", "EXPORTS",
+__all__ = ["KVCache", "rope3d", "segment_attn", "sparse_select", "segment_attn_sparse", "sparse_keep_count",
+           "device_error", "NomasError", "nomas_kvcache", "EXPORTS",
            "LIB_PATH"] + list(EXPORTS)

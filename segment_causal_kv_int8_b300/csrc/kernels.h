@@ -54,6 +54,29 @@ cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);
 // ------------------------------------------------------------------ self-test
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 
+// ------------------------------------------------------------------ sparse selection
+struct SparseSelectParams {
+  const void* kcache;            // cache K (int8 or bf16), [blocks*heads][cap_slots][128]
+  const float* kscale;           // int8 only
+  long long cap_slots;
+  int block_head_base;
+  int nc;                        // resident cache tokens
+  int n_tiles;                   // ceil(nc / 128)
+  const void* q;                 // bf16 [nq][heads][128]
+  int nq;
+  int heads;
+  int n_groups;                  // ceil(nq / 512)
+  int keep;                      // tiles kept per (head, group)
+  int max_keep;                  // row length of tiles
+  float* kbar;                   // workspace [heads][n_tiles][128]
+  float* qbar;                   // workspace [heads][n_groups][128]
+  int* tiles;                    // [heads][n_groups][max_keep]
+  int* counts;                   // [heads][n_groups]
+};
+
+size_t sparse_select_smem(int n_tiles);
+cudaError_t launch_sparse_select(bool int8_cache, const SparseSelectParams& p, cudaStream_t stream);
+
 // ------------------------------------------------------------------ attention
 struct AttnTensorMaps {
   CUtensorMap q, kcur, vcur, kc, vc;
@@ -76,6 +99,10 @@ struct AttnParams {
   const float* v_scale;
   long long scale_stride;        // cache slots per (block, head)
   uint32_t* err;                 // device error word
+  const int* sparse_tiles;       // nullable: [heads][groups][max_keep] kept cache tiles, increasing
+  const int* sparse_counts;      // [heads][groups]
+  int max_keep;
+  int n_groups;                  // 512-query groups (two 256-query blocks each)
 };
 
 cudaError_t launch_segment_attn(bool int8_cache, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,

@@ -400,10 +400,14 @@ NOMAS_API nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* c
   return NOMAS_OK;
 }
 
-NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const void* q, const void* k_cur,
-                                          const void* v_cur, int32_t n_video, int32_t n_text, float softmax_scale,
-                                          void* out, float* lse, void* workspace, size_t workspace_bytes,
-                                          int32_t num_splits, cudaStream_t stream) {
+namespace {
+// Dense attention (tiles == nullptr) or block-sparse attention over kept
+// cache-tile lists.  The split plan is the dense one either way, so both need
+// the workspace nomas_segment_attn_workspace_bytes reports.
+nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const void* q, const void* k_cur,
+                               const void* v_cur, int32_t n_video, int32_t n_text, float softmax_scale, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes, int32_t num_splits,
+                               const int32_t* tiles, const int32_t* counts, int32_t max_keep, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
   if (block < 0 || block >= cache->num_blocks || n_video < 0 || n_text < 0 || num_splits < 0)
@@ -421,6 +425,14 @@ NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t bl
   st = device_state(&err, &sms);
   if (st != NOMAS_OK) return st;
   AttnPlan pl = attn_plan(cache, n_video, n_text, num_splits, sms);
+  if (tiles != nullptr && num_splits == 0 && pl.splits > 1) {
+    // Block-sparse: plan for at most max_keep cache tiles per CTA, never more
+    // splits than the dense plan (whose workspace the caller sized).
+    const int eff = std::min(max_keep, pl.n_cache_tiles) + pl.n_cur_tiles;
+    const int s = std::max(1, std::min(auto_splits(pl.n_pairs * cache->heads, eff, cache->heads, pl.nq,
+                                                   sms > 0 ? sms : 148), eff));
+    if (s < pl.splits) pl = attn_plan(cache, n_video, n_text, s, sms);
+  }
   if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_o_bytes + pl.ws_lse_bytes ||
                         (reinterpret_cast<uintptr_t>(workspace) & 255u))) {
     if (num_splits > 1) return NOMAS_ERR_INVALID_ARG;  // an explicit split count needs its workspace
@@ -475,9 +487,97 @@ NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t bl
   p.v_scale = cache->v_scale;
   p.scale_stride = static_cast<long long>(cap_slots);
   p.err = err;
+  p.sparse_tiles = tiles;
+  p.sparse_counts = counts;
+  p.max_keep = max_keep;
+  p.n_groups = (pl.nq + 511) / 512;
   st = from_cuda(launch_segment_attn(int8, tm, p, pl.n_pairs, stream));
   if (st == NOMAS_OK && pl.splits > 1) st = from_cuda(launch_attn_combine(p, stream));
   return st;
+}
+
+int32_t sparse_keep_count(int32_t n_tiles, float keep_fraction) {
+  const double k = std::ceil(static_cast<double>(keep_fraction) * n_tiles - 1e-9);
+  return static_cast<int32_t>(std::min<double>(n_tiles, std::max(0.0, k)));
+}
+}  // namespace
+
+NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const void* q, const void* k_cur,
+                                          const void* v_cur, int32_t n_video, int32_t n_text, float softmax_scale,
+                                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                          int32_t num_splits, cudaStream_t stream) {
+  return segment_attn_impl(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, workspace,
+                           workspace_bytes, num_splits, nullptr, nullptr, 0, stream);
+}
+
+NOMAS_API nomas_status nomas_sparse_select_workspace_bytes(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
+                                                           size_t* bytes) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (bytes == nullptr || n_video < 0 || n_text < 0) return NOMAS_ERR_INVALID_ARG;
+  const int64_t nq = static_cast<int64_t>(n_video) + n_text;
+  const int64_t nc = static_cast<int64_t>(cache->valid_frames) * cache->grid_h * cache->grid_w;
+  const int64_t n_tiles = (nc + 127) / 128, n_groups = (nq + 511) / 512;
+  *bytes = round256(static_cast<size_t>(cache->heads) * n_tiles * 128 * 4) +
+           round256(static_cast<size_t>(cache->heads) * n_groups * 128 * 4);
+  return NOMAS_OK;
+}
+
+NOMAS_API nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t block, const void* q, int32_t n_video,
+                                           int32_t n_text, float keep_fraction, int32_t* tiles, int32_t* counts,
+                                           int32_t max_keep, void* workspace, size_t workspace_bytes,
+                                           cudaStream_t stream) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (block < 0 || block >= cache->num_blocks || n_video < 0 || n_text < 0) return NOMAS_ERR_INVALID_ARG;
+  if (q == nullptr || tiles == nullptr || counts == nullptr || !aligned16(q)) return NOMAS_ERR_INVALID_ARG;
+  if (!(keep_fraction > 0.0f) || !(keep_fraction <= 1.0f)) return NOMAS_ERR_INVALID_ARG;
+  const int64_t nq = static_cast<int64_t>(n_video) + n_text;
+  const int64_t nc = static_cast<int64_t>(cache->valid_frames) * cache->grid_h * cache->grid_w;
+  const int64_t n_tiles = (nc + 127) / 128, n_groups = (nq + 511) / 512;
+  if (n_tiles > 8192 || nq > (int64_t(1) << 28) || cache->heads > 65535) return NOMAS_ERR_UNSUPPORTED;
+  const int32_t keep = sparse_keep_count(static_cast<int32_t>(n_tiles), keep_fraction);
+  if (max_keep < keep) return NOMAS_ERR_INVALID_ARG;
+  size_t need = 0;
+  nomas_sparse_select_workspace_bytes(cache, n_video, n_text, &need);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return NOMAS_ERR_INVALID_ARG;
+  if (nq == 0) return NOMAS_OK;
+  SparseSelectParams p;
+  p.kcache = cache->k;
+  p.kscale = cache->k_scale;
+  p.cap_slots = static_cast<long long>(cache->grid_h) * cache->grid_w * cache->capacity_frames;
+  p.block_head_base = block * cache->heads;
+  p.nc = static_cast<int>(nc);
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.q = q;
+  p.nq = static_cast<int>(nq);
+  p.heads = cache->heads;
+  p.n_groups = static_cast<int>(n_groups);
+  p.keep = keep;
+  p.max_keep = max_keep;
+  p.kbar = static_cast<float*>(workspace);
+  p.qbar = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                    round256(static_cast<size_t>(cache->heads) * n_tiles * 128 * 4));
+  p.tiles = tiles;
+  p.counts = counts;
+  if (n_tiles == 0) {
+    // Nothing resident: every list is empty.
+    return from_cuda(cudaMemsetAsync(counts, 0, static_cast<size_t>(cache->heads) * n_groups * 4, stream));
+  }
+  return from_cuda(launch_sparse_select(cache->dtype == NOMAS_INT8, p, stream));
+}
+
+NOMAS_API nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int32_t block, const void* q,
+                                                 const void* k_cur, const void* v_cur, int32_t n_video, int32_t n_text,
+                                                 float softmax_scale, const int32_t* tiles, const int32_t* counts,
+                                                 int32_t max_keep, void* out, float* lse, void* workspace,
+                                                 size_t workspace_bytes, int32_t num_splits, cudaStream_t stream) {
+  if (tiles == nullptr || counts == nullptr || max_keep <= 0) return NOMAS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(tiles) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u))
+    return NOMAS_ERR_INVALID_ARG;
+  return segment_attn_impl(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, workspace,
+                           workspace_bytes, num_splits, tiles, counts, max_keep, stream);
 }
 
 NOMAS_API nomas_status nomas_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {

@@ -88,15 +88,42 @@ struct TileInfo {
   int valid;
 };
 
-__device__ __forceinline__ TileInfo tile_info(int j, const AttnParams& p) {
+// The key tiles a CTA visits, in order: n_cache cache tiles (all resident
+// ones, or the kept list of block-sparse attention), then every current tile.
+struct KeyTiles {
+  int n_cache;
+  const int* list;  // null: cache tiles 0 .. n_cache-1
+};
+
+__device__ __forceinline__ KeyTiles key_tiles(const AttnParams& p, int head) {
+  KeyTiles kt;
+  if (p.sparse_tiles == nullptr) {
+    kt.n_cache = p.n_cache_tiles;
+    kt.list = nullptr;
+  } else {
+    // Query group = two consecutive 256-query blocks (one CTA pair for INT8).
+    const size_t hg = static_cast<size_t>(head) * p.n_groups + (blockIdx.x >> 1);
+    kt.n_cache = min(max(p.sparse_counts[hg], 0), min(p.max_keep, p.n_cache_tiles));
+    kt.list = p.sparse_tiles + hg * p.max_keep;
+  }
+  return kt;
+}
+
+__device__ __forceinline__ TileInfo tile_info(int j, const AttnParams& p, const KeyTiles& kt) {
   TileInfo t;
-  if (j < p.n_cache_tiles) {
+  if (j < kt.n_cache) {
+    int c = kt.list ? kt.list[j] : j;
+    if (c < 0 || c >= p.n_cache_tiles) {
+      // A bad list entry: stay inside the cache and report it.
+      if (p.err) atomicCAS(p.err, 0u, 1u /* NOMAS_ERR_INVALID_ARG */);
+      c = min(max(c, 0), p.n_cache_tiles - 1);
+    }
     t.cache = true;
-    t.row0 = j * 128;
+    t.row0 = c * 128;
     t.valid = min(128, p.nc - t.row0);
   } else {
     t.cache = false;
-    t.row0 = (j - p.n_cache_tiles) * 128;
+    t.row0 = (j - kt.n_cache) * 128;
     t.valid = min(128, p.nq - t.row0);
   }
   return t;
@@ -124,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int head = blockIdx.y;
   const int split = blockIdx.z;
   const int q_row0 = blockIdx.x * 256;
-  const int n_tiles = p.n_cache_tiles + p.n_cur_tiles;
+  const KeyTiles kt = key_tiles(p, head);
+  const int n_tiles = kt.n_cache + p.n_cur_tiles;
   const int t_begin = static_cast<int>((static_cast<long long>(split) * n_tiles) / p.num_splits);
   const int t_end = static_cast<int>((static_cast<long long>(split + 1) * n_tiles) / p.num_splits);
   const int n_iter = t_end - t_begin;
@@ -196,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     for (int it = 0; it < n_iter && ok; ++it) {
-      const TileInfo ti = tile_info(t_begin + it, p);
+      const TileInfo ti = tile_info(t_begin + it, p, kt);
       for (int kv = 0; kv < 2 && ok; ++kv) {
         const int r = 2 * it + kv;
         if constexpr (kInt8) {
@@ -374,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t lacc[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial row sums (0.0f bits are 0)
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
-      const int valid = tile_info(t_begin + it, p).valid;
+      const int valid = tile_info(t_begin + it, p, kt).valid;
       if (!warp_wait(&bars[L::bSFull + t], it & 1, ab, p.err)) {
         ok = false;
         break;
@@ -493,6 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (live) p.ws_lse[(static_cast<size_t>(split) * p.heads + head) * p.nq + grow] = lse_val;
       }
+    } else if (ok && n_iter == 0 && p.num_splits > 1) {
+      // A split with no key tile (a block-sparse list shorter than the split
+      // count) contributes weight zero to the combine: O = 0, LSE = -inf.
+      const int grow = q_row0 + t * 128 + row;
+      if (grow < p.nq) {
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + ((static_cast<size_t>(split) * p.heads + head) * p.nq + grow) * 128);
+#pragma unroll 4
+        for (int c = 0; c < 32; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.ws_lse[(static_cast<size_t>(split) * p.heads + head) * p.nq + grow] = -INFINITY;
+      }
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ ring filler (INT8 cache)
@@ -516,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ri = 0, r_tma = 0;
       bool ok = true;
       for (int it = 0; it < n_iter && ok; ++it) {
-        const TileInfo ti = tile_info(t_begin + it, p);
+        const TileInfo ti = tile_info(t_begin + it, p, kt);
         for (int kv = 0; kv < 2; ++kv) {
           const int r = 2 * it + kv, s = r % L::NS, u = r / L::NS;
           uint64_t* fb = &bars[L::bRingFull + s];
@@ -601,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && warp == 12) {
         // Abort: give the current-tile copies this warp issued time to land.
         for (int r = r_tma - 1; r >= 0 && r >= r_tma - L::NS; --r) {
-          const TileInfo ti = tile_info(t_begin + r / 2, p);
+          const TileInfo ti = tile_info(t_begin + r / 2, p, kt);
           if (ti.cache) continue;
           warp_wait_teardown(&bars[L::bRingFull + r % L::NS], (r / L::NS) & 1, 20000000ull);
         }
