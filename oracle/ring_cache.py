@@ -34,6 +34,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import int8_codec
+from .rope3d import rope3d_segment
 
 
 class CapacityError(RuntimeError):
@@ -131,6 +132,31 @@ class RingCache:
         self.total_frames += n_frames
         self.valid_frames = min(self.total_frames, self.window)
         return plan
+
+    def append_rope(self, k, v, theta: float = 10000.0, split=(32, 48, 48)):
+        """Append a finished segment whose keys still lack their 3D RoPE.
+
+        After a segment is generated its keys and values are written to the
+        cache (the KV-write stage, Hy-Nomas auf einer RTX 4090, section
+        "Zeiten"), and later segments see them at their own positions, which
+        continue from the cached frames.  Reading: frame ``f`` of the segment is
+        rotated at ``(total_frames + f, h, w)`` (as :func:`rope3d_segment` with
+        ``t0 = total_frames``) in float64, rounded once to float32 (the
+        precision in which a stored row is quantised or rounded to bf16), and
+        then appended as by :meth:`append`; V is appended unchanged.  Frames
+        the window drops at once keep their absolute positions: only the
+        resident ones are written.
+        """
+        k = np.asarray(k, dtype=np.float64)
+        if k.ndim == 3:
+            k = k[None]
+        if k.shape[1] % self.tpf:
+            raise ValueError("token count is not a whole number of frames")
+        frames = k.shape[1] // self.tpf
+        rot = np.stack([rope3d_segment(k[b], frames, self.grid_h, self.grid_w, self.total_frames, theta, split)
+                        for b in range(k.shape[0])])
+        v = np.asarray(v)
+        return self.append(rot.astype(np.float32), v[None] if v.ndim == 3 else v)
 
     def resident_frames(self):
         """Absolute latent frames resident on the device, oldest first."""
