@@ -543,12 +543,27 @@ def _load_traffic(config):
 
 
 # ------------------------------------------------------------------ session workload
-def session_flops(wl, turns: int) -> float:
-    """Attention FLOPs of a session: every turn runs steps x blocks calls over the cache resident then."""
+def session_flops(wl, turns: int, keep: float = 0.0, dense_steps: int = 2) -> float:
+    """Attention FLOPs of a session: every turn runs steps x blocks calls over the cache resident then.
+
+    With ``keep`` (block-sparse after ``dense_steps`` dense steps) the sparse
+    calls count ceil(keep * T) kept tiles of 128 keys per query group (capped
+    at the resident keys): an upper bound, since a kept partial last tile
+    holds fewer keys.
+    """
+    import math
     total = 0.0
     for t in range(turns):
-        n_k = min(t * wl.cur_frames, wl.window) * wl.tpf + wl.n_q
-        total += wl.steps * wl.blocks * 4.0 * wl.n_q * n_k * wl.head_dim * wl.heads
+        n_c = min(t * wl.cur_frames, wl.window) * wl.tpf
+        dense = 4.0 * wl.n_q * (n_c + wl.n_q) * wl.head_dim * wl.heads
+        if not keep:
+            total += wl.steps * wl.blocks * dense
+            continue
+        n_t = -(-n_c // 128)
+        kept = min(n_c, 128 * min(n_t, math.ceil(keep * n_t - 1e-9)))
+        sparse = 4.0 * wl.n_q * (kept + wl.n_q) * wl.head_dim * wl.heads
+        n_dense = min(dense_steps, wl.steps)
+        total += wl.blocks * (n_dense * dense + (wl.steps - n_dense) * sparse)
     return total
 
 
@@ -589,6 +604,18 @@ def run_session(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     calls = [0]
+    keep = args.sparse
+    if keep:
+        # Block-sparse after two dense steps: per block a kept-tile list and
+        # the mean keys of its window (computed at the first sparse step of a
+        # turn, reused by the later ones while the cache is unchanged).
+        n_tiles_max = -(-wl.window * wl.tpf // 128)
+        groups = -(-wl.n_q // 512)
+        sel_tiles = torch.zeros((wl.heads, groups, max(1, nomas.sparse_keep_count(n_tiles_max, keep))),
+                                dtype=torch.int32, device=dev)
+        sel_counts = torch.zeros((wl.heads, groups), dtype=torch.int32, device=dev)
+        kbar_bytes = -(-wl.heads * n_tiles_max * 128 * 4 // 256) * 256
+        kbar = torch.empty((wl.blocks, kbar_bytes), dtype=torch.uint8, device=dev)
     archive = None
     if args.archive:
         # Host KV archive of every appended frame (pinned, one session's worth).
@@ -603,8 +630,16 @@ def run_session(args):
                     q, k, v = pool[(s * wl.blocks + blk) % len(pool)]
                     nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, cache.total_frames, wl.theta,
                                  wl.rope_split)
-                    nomas.segment_attn(cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
-                    calls[0] += 2
+                    if keep and s >= 2 and cache.valid_frames > 0:
+                        nomas.sparse_select(cache, blk, q, wl.n_video, wl.n_text, keep, tiles=sel_tiles,
+                                            counts=sel_counts, workspace=kbar[blk], reuse_key_means=s > 2)
+                        nomas.segment_attn_sparse(cache, blk, q, k, v, wl.n_video, wl.n_text, sel_tiles, sel_counts,
+                                                  out=out, workspace=ws)
+                        calls[0] += 3 + (1 if s == 2 else 0)
+                    else:
+                        nomas.segment_attn(cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
+                        calls[0] += 1
+                    calls[0] += 1
             if archive is not None:
                 used = cache.append_archive(seg_k, seg_v, archive, used)
             else:
@@ -631,7 +666,7 @@ def run_session(args):
         dist.barrier()
     clocks = sampler.stop()
     total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
-    flops = session_flops(wl, turns)
+    flops = session_flops(wl, turns, keep)
     value = whole_job_value(flops, world, args.steps, total_ms)
     peaks, src = load_peaks()
     if rank == 0:
@@ -652,6 +687,13 @@ def run_session(args):
                          "peak_source": f"bf16_tflops_sustained of {src} peaks (a seconds-long step)"},
             "gpu_launches": calls[0], "clocks": clocks,
         }
+        if keep:
+            line["config"]["workload"] += (f"; steps 0-1 dense, steps 2-{wl.steps - 1} block-sparse keeping {keep} "
+                                           "of the cache tiles (mean keys computed once per turn and block)")
+            line["sparse"] = {"keep": keep, "executed_flops_upper_bound": flops,
+                              "dense_flops": session_flops(wl, turns),
+                              "dense_equivalent_tflops": whole_job_value(session_flops(wl, turns), world,
+                                                                         args.steps, total_ms)}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -161,6 +161,27 @@ nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k, const voi
                                   int64_t block_stride_elems, cudaStream_t stream);
 
 /*
+ * The KV-write stage with position encoding (the "Schreiben des KV-Cache"
+ * stage of the RTX 4090 guide, section "Zeiten"; positions continue from the
+ * cached frames): nomas_kvcache_append of a segment whose keys have not been
+ * rotated yet.  Frame f of the segment is rotated by 3D RoPE at positions
+ * (total_frames + f, h, w) in float32, with the pair layout and frequencies of
+ * nomas_rope3d_apply (theta, d_t, d_h, d_w as there), and the rotated row is
+ * then quantised (INT8) or rounded to bf16 like any appended row; V is
+ * appended unchanged.  One pass over the input instead of a RoPE pass over K
+ * followed by an append.  With float32 input the stored bits equal those of
+ * nomas_rope3d_apply (t0 = total_frames) followed by nomas_kvcache_append;
+ * with bf16 input the rotated keys are not rounded to bf16 before they are
+ * stored.  Arguments, errors and metadata updates as nomas_kvcache_append,
+ * plus NOMAS_ERR_INVALID_ARG for a bad rotary split or theta and
+ * NOMAS_ERR_UNSUPPORTED when total_frames + n_frames reaches 2^24.
+ */
+nomas_status nomas_kvcache_append_rope(nomas_kvcache* cache, const void* k, const void* v,
+                                       nomas_dtype in_dt, int32_t n_frames,
+                                       int64_t block_stride_elems, float theta, int32_t d_t,
+                                       int32_t d_h, int32_t d_w, cudaStream_t stream);
+
+/*
  * Host archive of every appended frame (the CPU KV archive of the low-memory
  * recipe: the GPU keeps the last past_frames latent frames, all earlier ones
  * live in host RAM; "System-RAM" on the inferencekey.com RTX 4090 test page
@@ -239,7 +260,8 @@ nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const
  * lower tile first), listed in increasing tile order.
  *
  * nomas_sparse_select_workspace_bytes: device scratch nomas_sparse_select
- * needs (the mean keys and mean queries, float32).  Host only.
+ * needs: the mean keys, float32 [heads][T][head_dim], 256-byte rounded.
+ * Host only.
  *
  * nomas_sparse_select: compute the kept lists for one block.
  *   q               device bf16 [n_video + n_text][heads][head_dim] (the
@@ -250,6 +272,13 @@ nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const
  *                   of the row is left untouched
  *   counts          device int32 [heads][groups], groups = ceil((n_video + n_text) / 512)
  *   max_keep        row length of `tiles`; must be >= k
+ *   reuse_key_means 0: compute the mean keys of the resident cache into the
+ *                   workspace (one pass over the cache K).  Non-zero: the
+ *                   workspace still holds the mean keys an earlier call
+ *                   computed for this block with the cache unchanged since
+ *                   (no append or reset), as across the denoising steps of
+ *                   one turn; only the queries are read.  Stale means give a
+ *                   valid but different list.
  *   workspace       device scratch, 256-byte aligned, of at least the bytes
  *                   nomas_sparse_select_workspace_bytes reports
  * Returns NOMAS_ERR_INVALID_ARG (nothing enqueued) for a bad argument and
@@ -271,7 +300,8 @@ nomas_status nomas_sparse_select_workspace_bytes(const nomas_kvcache* cache, int
 nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t block, const void* q,
                                  int32_t n_video, int32_t n_text, float keep_fraction,
                                  int32_t* tiles, int32_t* counts, int32_t max_keep,
-                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                                 int32_t reuse_key_means, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
 nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int32_t block, const void* q,
                                        const void* k_cur, const void* v_cur, int32_t n_video,
                                        int32_t n_text, float softmax_scale, const int32_t* tiles,

@@ -77,6 +77,8 @@ EXPORTS = {
     "nomas_rope3d_apply": (_c_int, [_vp, _vp, _c_int, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i64, _f32,
                                     _i32, _i32, _i32, _vp]),
     "nomas_kvcache_append": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _vp]),
+    "nomas_kvcache_append_rope": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _f32, _i32, _i32, _i32,
+                                           _vp]),
     "nomas_kvcache_archive_frame_bytes": (_sz, [_P(nomas_kvcache)]),
     "nomas_kvcache_append_archive": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _vp, _sz, _P(_sz),
                                               _vp]),
@@ -86,8 +88,8 @@ EXPORTS = {
     "nomas_segment_attn_noalloc": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
                                             _i32, _vp]),
     "nomas_sparse_select_workspace_bytes": (_c_int, [_P(nomas_kvcache), _i32, _i32, _P(_sz)]),
-    "nomas_sparse_select": (_c_int, [_P(nomas_kvcache), _i32, _vp, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _sz,
-                                     _vp]),
+    "nomas_sparse_select": (_c_int, [_P(nomas_kvcache), _i32, _vp, _i32, _i32, _f32, _vp, _vp, _i32, _i32, _vp,
+                                     _sz, _vp]),
     "nomas_segment_attn_sparse": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
                                            _i32, _vp, _vp, _vp, _sz, _i32, _vp]),
     "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
@@ -203,6 +205,21 @@ class KVCache:
 
     def append(self, k, v, stream=None) -> None:
         """Append a finished segment: ``k``, ``v`` ``[blocks][F*tpf][heads][128]`` (or 3-D for one block)."""
+        k, v = self._check_segment(k, v)
+        _check(nomas_kvcache_append(ctypes.byref(self.desc), ctypes.c_void_p(k.data_ptr()),
+                                    ctypes.c_void_p(v.data_ptr()), _dt_code(k), k.shape[1] // self.tpf,
+                                    k.stride(0), _stream_ptr(stream)), "nomas_kvcache_append")
+
+    def append_rope(self, k, v, theta: float = 10000.0, split=(32, 48, 48), stream=None) -> None:
+        """Append a segment whose keys are not yet position-encoded: K is rotated by 3D RoPE at
+        (total_frames + f, h, w) on the way into the cache."""
+        k, v = self._check_segment(k, v)
+        _check(nomas_kvcache_append_rope(ctypes.byref(self.desc), ctypes.c_void_p(k.data_ptr()),
+                                         ctypes.c_void_p(v.data_ptr()), _dt_code(k), k.shape[1] // self.tpf,
+                                         k.stride(0), theta, split[0], split[1], split[2], _stream_ptr(stream)),
+               "nomas_kvcache_append_rope")
+
+    def _check_segment(self, k, v):
         if k.dim() == 3:
             k, v = k.unsqueeze(0), v.unsqueeze(0)
         if k.shape != v.shape or k.dtype != v.dtype or not k.is_cuda:
@@ -216,9 +233,7 @@ class KVCache:
                 raise ValueError("K/V rows must be contiguous within a block")
         if k.stride() != v.stride():
             raise ValueError("k and v must share strides")
-        _check(nomas_kvcache_append(ctypes.byref(self.desc), ctypes.c_void_p(k.data_ptr()),
-                                    ctypes.c_void_p(v.data_ptr()), _dt_code(k), k.shape[1] // self.tpf,
-                                    k.stride(0), _stream_ptr(stream)), "nomas_kvcache_append")
+        return k, v
 
     def archive_frame_bytes(self) -> int:
         return int(nomas_kvcache_archive_frame_bytes(ctypes.byref(self.desc)))
@@ -297,12 +312,14 @@ def sparse_keep_count(n_tiles: int, keep_fraction: float) -> int:
 
 
 def sparse_select(cache: KVCache, block: int, q, n_video: int, n_text: int, keep_fraction: float = 0.25,
-                  tiles=None, counts=None, workspace=None, stream=None):
+                  tiles=None, counts=None, workspace=None, reuse_key_means: bool = False, stream=None):
     """Kept cache tiles of block-sparse attention; returns ``(tiles, counts)``.
 
     ``tiles``: int32 ``[heads][groups][max_keep]`` (first ``counts[h, g]``
     entries of a row valid, increasing), ``counts``: int32 ``[heads][groups]``,
     groups = ceil((n_video + n_text) / 512).  Allocated when not given.
+    ``reuse_key_means``: ``workspace`` still holds the mean keys of an earlier
+    call on this block with the cache unchanged since.
     """
     torch = _torch()
     if not q.is_cuda or q.dtype != torch.bfloat16 or not q.is_contiguous():
@@ -321,10 +338,12 @@ def sparse_select(cache: KVCache, block: int, q, n_video: int, n_text: int, keep
     _check(nomas_sparse_select_workspace_bytes(ctypes.byref(cache.desc), n_video, n_text, ctypes.byref(need)),
            "nomas_sparse_select_workspace_bytes")
     if workspace is None:
+        if reuse_key_means:
+            raise ValueError("reuse_key_means needs the workspace of the earlier call")
         workspace = torch.empty(max(256, need.value), dtype=torch.uint8, device=q.device)
     _check(nomas_sparse_select(ctypes.byref(cache.desc), block, ctypes.c_void_p(q.data_ptr()), n_video, n_text,
                                keep_fraction, ctypes.c_void_p(tiles.data_ptr()), ctypes.c_void_p(counts.data_ptr()),
-                               tiles.shape[-1], ctypes.c_void_p(workspace.data_ptr()),
+                               tiles.shape[-1], int(bool(reuse_key_means)), ctypes.c_void_p(workspace.data_ptr()),
                                workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "nomas_sparse_select")
     return tiles, counts

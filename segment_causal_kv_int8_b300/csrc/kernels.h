@@ -47,6 +47,10 @@ struct AppendParams {
 };
 
 cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, int sms, cudaStream_t stream);
+// Append with 3D RoPE of the K rows (rp.t0 = absolute frame of the first
+// written frame; rp.tpf, rp.grid_w and the pair tables set).
+cudaError_t launch_append_rope(bool f32_in, bool int8_cache, const AppendParams& p, const RopeParams& rp,
+                               cudaStream_t stream);
 
 // ------------------------------------------------------------------ reset
 cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);
@@ -69,13 +73,13 @@ struct SparseSelectParams {
   int keep;                      // tiles kept per (head, group)
   int max_keep;                  // row length of tiles
   float* kbar;                   // workspace [heads][n_tiles][128]
-  float* qbar;                   // workspace [heads][n_groups][128]
   int* tiles;                    // [heads][n_groups][max_keep]
   int* counts;                   // [heads][n_groups]
 };
 
 size_t sparse_select_smem(int n_tiles);
-cudaError_t launch_sparse_select(bool int8_cache, const SparseSelectParams& p, cudaStream_t stream);
+cudaError_t launch_sparse_select(bool int8_cache, bool reuse_key_means, const SparseSelectParams& p,
+                                 cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention
 struct AttnTensorMaps {

@@ -25,6 +25,7 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "rope_math.cuh"
 #include "sm100.cuh"
 
 namespace nomas {
@@ -100,6 +101,71 @@ __device__ __forceinline__ void write_row(const AppendParams& p, int tensor, lon
       u[e] = *reinterpret_cast<const uint32_t*>(&t);
     }
     *reinterpret_cast<uint4*>(dst) = w;
+  }
+}
+
+// Quantise (or round to bf16) one row from 16 values per lane of an 8-lane
+// group and write it to its ring slot.
+template <bool kInt8>
+__device__ __forceinline__ void store_row16(const AppendParams& p, int tensor, long long dst_row, const float (&x)[16],
+                                            int g, unsigned gmask) {
+  if constexpr (kInt8) {
+    float m0 = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    float m1 = fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7])));
+    float m2 = fmaxf(fmaxf(fabsf(x[8]), fabsf(x[9])), fmaxf(fabsf(x[10]), fabsf(x[11])));
+    float m3 = fmaxf(fmaxf(fabsf(x[12]), fabsf(x[13])), fmaxf(fabsf(x[14]), fabsf(x[15])));
+    float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
+    const float scale = __fdiv_rn(m, 127.0f);
+    const float inv = __fdiv_rn(127.0f, m);
+    uint32_t c[4];
+    if (inv <= 3.0e38f) {
+      // rint(fl32(x * inv)) in [-127, 127]: adding 1.5 * 2^23 rounds to an
+      // integer (ties to even) whose low byte is the two's-complement code.
+      // The product is rounded on its own (the packed multiply) and the add
+      // is a separate scalar __fadd_rn, so nothing fuses the two into an FMA.
+      const uint64_t inv2 = f2_pack(inv, inv);
+      uint32_t bb[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float y0, y1;
+        f2_unpack(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), y0, y1);
+        bb[2 * e] = __float_as_uint(__fadd_rn(y0, 12582912.0f));
+        bb[2 * e + 1] = __float_as_uint(__fadd_rn(y1, 12582912.0f));
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        c[q] = __byte_perm(__byte_perm(bb[4 * q], bb[4 * q + 1], 0x0040), __byte_perm(bb[4 * q + 2], bb[4 * q + 3], 0x0040),
+                           0x5410);
+    } else {
+      // inv overflowed (absmax below 127 / FLT_MAX): +-inf products clamp to
+      // +-127 and NaN (0 * inf) converts to 0.
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        c[q] = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          int ci = __float2int_rn(__fmul_rn(x[4 * q + e], inv));
+          ci = max(-127, min(127, ci));
+          c[q] |= (static_cast<uint32_t>(ci) & 0xFFu) << (8 * e);
+        }
+      }
+    }
+    int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
+    if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
+  } else {
+    uint4 o[2];
+    uint32_t* u = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      __nv_bfloat162 t = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+      u[e] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g);
+    dst[0] = o[0];
+    dst[1] = o[1];
   }
 }
 
@@ -187,51 +253,7 @@ __global__ void __launch_bounds__(256, kInt8 ? 6 : 8) append8_kernel(const __gri
         x[2 * e] = __uint_as_float(u[e] << 16);
         x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
       }
-      float m0 = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-      float m1 = fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7])));
-      float m2 = fmaxf(fmaxf(fabsf(x[8]), fabsf(x[9])), fmaxf(fabsf(x[10]), fabsf(x[11])));
-      float m3 = fmaxf(fmaxf(fabsf(x[12]), fabsf(x[13])), fmaxf(fabsf(x[14]), fabsf(x[15])));
-      float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-#pragma unroll
-      for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
-      const float scale = __fdiv_rn(m, 127.0f);
-      const float inv = __fdiv_rn(127.0f, m);
-      uint32_t c[4];
-      if (inv <= 3.0e38f) {
-        // rint(fl32(x * inv)) in [-127, 127]: adding 1.5 * 2^23 rounds to an
-        // integer (ties to even) whose low byte is the two's-complement code.
-        // The product is rounded on its own (the packed multiply) and the add
-        // is a separate scalar __fadd_rn, so nothing fuses the two into an FMA.
-        const uint64_t inv2 = f2_pack(inv, inv);
-        uint32_t bb[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float y0, y1;
-          f2_unpack(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), y0, y1);
-          bb[2 * e] = __float_as_uint(__fadd_rn(y0, 12582912.0f));
-          bb[2 * e + 1] = __float_as_uint(__fadd_rn(y1, 12582912.0f));
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          c[q] = __byte_perm(__byte_perm(bb[4 * q], bb[4 * q + 1], 0x0040), __byte_perm(bb[4 * q + 2], bb[4 * q + 3], 0x0040),
-                             0x5410);
-      } else {
-        // inv overflowed (absmax below 127 / FLT_MAX): +-inf products clamp to
-        // +-127 and NaN (0 * inf) converts to 0.
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          c[q] = 0;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            int ci = __float2int_rn(__fmul_rn(x[4 * q + e], inv));
-            ci = max(-127, min(127, ci));
-            c[q] |= (static_cast<uint32_t>(ci) & 0xFFu) << (8 * e);
-          }
-        }
-      }
-      int8_t* dst = static_cast<int8_t*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
-      if (g == 0) (tensor ? p.vs : p.ks)[dst_row] = scale;
+      store_row16<true>(p, tensor, dst_row, x, g, gmask);
     } else {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g);
       dst[0] = w[r][0];
@@ -349,6 +371,157 @@ __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const 
   }
 }
 
+// Fused 3D RoPE + append (the KV-write stage): K rows are rotated in float32
+// at their absolute positions (latent frame t0 + f, h, w) and then quantised
+// or copied like any other row; V rows are appended unchanged.  A CTA covers
+// kRopeAppendTokens consecutive tokens of 16 heads: it issues all its loads,
+// computes the cos/sin of its tokens' rotary pairs once into shared memory
+// (shared by the 16 heads), then rotates, quantises and writes.  With float32
+// input the rotation is the RoPE kernel's arithmetic, so the cache receives
+// exactly what RoPE followed by append would write.
+constexpr int kRopeAppendTokens = 8;
+
+template <bool kF32In, bool kInt8>
+__global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant__ AppendParams p,
+                                                          const __grid_constant__ RopeParams rp, TwoPi tp) {
+  __shared__ float2 cs[kRopeAppendTokens][kRopeMaxPairs];  // (cos, sin) per token and pair
+  const int h = blockIdx.y * 16 + (threadIdx.x >> 4);
+  const bool live = h < p.heads;
+  const int g = threadIdx.x & 15;
+  const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
+  const int tensor = blockIdx.z & 1;
+  const int b = blockIdx.z >> 1;
+  const int n0 = blockIdx.x * kRopeAppendTokens;
+  const void* src = tensor ? p.v : p.k;
+  const long long plane = static_cast<long long>(b) * p.heads + h;
+  float x[kRopeAppendTokens][8];
+  if (live) {
+#pragma unroll
+    for (int r = 0; r < kRopeAppendTokens; ++r) {
+      const int n = n0 + r;
+      if (n < p.n_tokens) {
+        const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
+        load8<kF32In>(src, b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g, x[r]);
+      }
+    }
+  }
+  if (tensor == 0) {
+    for (int i = threadIdx.x; i < kRopeAppendTokens * kRopeMaxPairs; i += blockDim.x) {
+      const int r = i / kRopeMaxPairs, pair = i - r * kRopeMaxPairs;
+      const int n = n0 + r;
+      const int a = rp.axis[pair];
+      float c = 1.0f, sn = 0.0f;
+      if (n < p.n_tokens && a >= 0) {
+        const int f = n / p.tpf;
+        const int within = n - f * p.tpf;
+        const int row = within / rp.grid_w;
+        const float pos = a == 0 ? static_cast<float>(rp.t0 + f)
+                                 : static_cast<float>(a == 1 ? row : within - row * rp.grid_w);
+        sincosf(rope_reduced_angle(pos, rp.f_hi[pair], rp.f_lo[pair], tp), &sn, &c);
+      }
+      cs[r][pair] = make_float2(c, sn);
+    }
+    __syncthreads();  // tensor is uniform over the CTA
+  }
+  if (!live) return;  // whole 16-lane groups leave together
+#pragma unroll
+  for (int r = 0; r < kRopeAppendTokens; ++r) {
+    const int n = n0 + r;
+    if (n >= p.n_tokens) break;
+    if (tensor == 0) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 t = cs[r][4 * g + e];
+        rope_rotate_pair(x[r][2 * e], x[r][2 * e + 1], t.x, t.y);
+      }
+    }
+    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    int slot_frame = p.base_slot_frame + f;
+    if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
+    const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
+    write_row<kInt8>(p, tensor, dst_row, x[r], g, gmask);
+  }
+}
+
+// Fused RoPE + append for bf16 input, in the 8-lanes-per-row layout of
+// append8_kernel (lane g holds values 16g .. 16g+15, i.e. rotary pairs
+// 8g .. 8g+7).  A CTA takes 64 consecutive (token, head) rows of the input,
+// which is one contiguous 16 KB range, two rows per 8-lane group; the cos/sin
+// of the tokens those rows belong to are computed once into shared memory.
+constexpr int kRope8Rows = 64;
+constexpr int kRope8MaxTokens = kRope8Rows + 1;  // tokens a 64-row range can touch (heads = 1)
+
+template <bool kInt8>
+__global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_constant__ AppendParams p,
+                                                              const __grid_constant__ RopeParams rp, TwoPi tp) {
+  __shared__ float2 cs[kRope8MaxTokens][kRopeMaxPairs];
+  const int g = threadIdx.x & 7;
+  const unsigned gmask = 0xFFu << (threadIdx.x & 24);
+  const int tensor = blockIdx.z & 1;
+  const int b = blockIdx.z >> 1;
+  const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
+  const long long r0 = static_cast<long long>(blockIdx.x) * kRope8Rows;
+  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(tensor ? p.v : p.k) + b * p.block_stride +
+                             static_cast<long long>(p.first_frame) * p.tpf * p.heads * 128;
+  uint4 w[2][2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const long long row = r0 + (threadIdx.x >> 3) + 32 * r;
+    if (row < rows) {
+      const uint4* q = reinterpret_cast<const uint4*>(src + row * 128 + 16 * g);
+      w[r][0] = q[0];
+      w[r][1] = q[1];
+    }
+  }
+  const int tok0 = static_cast<int>(r0 / p.heads);
+  if (tensor == 0) {
+    const int n_tok = static_cast<int>(min(rows - 1, r0 + kRope8Rows - 1) / p.heads) - tok0 + 1;
+    for (int i = threadIdx.x; i < n_tok * kRopeMaxPairs; i += blockDim.x) {
+      const int t = i / kRopeMaxPairs, pair = i - t * kRopeMaxPairs;
+      const int n = tok0 + t;
+      const int a = rp.axis[pair];
+      float c = 1.0f, sn = 0.0f;
+      if (a >= 0) {
+        const int f = n / p.tpf;
+        const int within = n - f * p.tpf;
+        const int hrow = within / rp.grid_w;
+        const float pos = a == 0 ? static_cast<float>(rp.t0 + f)
+                                 : static_cast<float>(a == 1 ? hrow : within - hrow * rp.grid_w);
+        sincosf(rope_reduced_angle(pos, rp.f_hi[pair], rp.f_lo[pair], tp), &sn, &c);
+      }
+      cs[t][pair] = make_float2(c, sn);
+    }
+    __syncthreads();  // tensor is uniform over the CTA
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const long long row = r0 + (threadIdx.x >> 3) + 32 * r;
+    if (row >= rows) break;  // rows of one 8-lane group: uniform
+    const int n = static_cast<int>(row / p.heads);
+    const int h = static_cast<int>(row - static_cast<long long>(n) * p.heads);
+    const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
+    float x[16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      x[2 * e] = __uint_as_float(u[e] << 16);
+      x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+    }
+    if (tensor == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 t = cs[n - tok0][8 * g + e];
+        rope_rotate_pair(x[2 * e], x[2 * e + 1], t.x, t.y);
+      }
+    }
+    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    int slot_frame = p.base_slot_frame + f;
+    if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
+    const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
+                              static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
+    store_row16<kInt8>(p, tensor, dst_row, x, g, gmask);
+  }
+}
+
 __global__ void __launch_bounds__(256) zero_fill_kernel(uint8_t* __restrict__ ptr, size_t bytes) {
   const size_t n16 = bytes / 16;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -359,6 +532,31 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint8_t* __restrict__ pt
 }
 
 }  // namespace
+
+cudaError_t launch_append_rope(bool f32_in, bool int8_cache, const AppendParams& p, const RopeParams& rp,
+                               cudaStream_t stream) {
+  if (p.n_tokens <= 0 || p.blocks <= 0 || p.heads <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((p.n_tokens + kRopeAppendTokens - 1) / kRopeAppendTokens),
+                  static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
+  if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+  const TwoPi tp = rope_two_pi();
+  if (f32_in) {
+    if (int8_cache)
+      append_rope_kernel<true, true><<<grid, 256, 0, stream>>>(p, rp, tp);
+    else
+      append_rope_kernel<true, false><<<grid, 256, 0, stream>>>(p, rp, tp);
+  } else {
+    const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
+    const long long cta = (rows + kRope8Rows - 1) / kRope8Rows;
+    if (cta > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const dim3 grid8(static_cast<unsigned>(cta), 1, static_cast<unsigned>(2 * p.blocks));
+    if (int8_cache)
+      append8_rope_kernel<true><<<grid8, 256, 0, stream>>>(p, rp, tp);
+    else
+      append8_rope_kernel<false><<<grid8, 256, 0, stream>>>(p, rp, tp);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p_in, int sms, cudaStream_t stream) {
   if (p_in.n_tokens <= 0 || p_in.blocks <= 0 || p_in.heads <= 0) return cudaSuccess;

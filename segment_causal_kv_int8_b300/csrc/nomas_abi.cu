@@ -209,6 +209,30 @@ NOMAS_API nomas_status nomas_kvcache_plan_append(const nomas_kvcache* cache, int
   return plan(cache, n_frames, first_frame, slot_frame, new_total, new_valid);
 }
 
+namespace {
+// Pair tables of 3D RoPE: axis chunks of d_t, d_h, d_w dims in that order,
+// pair i of a chunk of d_a dims at frequency theta^(-2i/d_a) (two floats).
+void rope_tables(RopeParams* p, float theta, int32_t d_t, int32_t d_h, int32_t d_w) {
+  memset(p, 0, sizeof(*p));
+  const int dims[3] = {d_t, d_h, d_w};
+  int pair = 0;
+  for (int a = 0; a < 3; ++a) {
+    for (int i = 0; i < dims[a] / 2; ++i, ++pair) {
+      const double f = pow(static_cast<double>(theta), -2.0 * i / dims[a]);
+      p->f_hi[pair] = static_cast<float>(f);
+      p->f_lo[pair] = static_cast<float>(f - static_cast<double>(p->f_hi[pair]));
+      p->axis[pair] = static_cast<int8_t>(a);
+    }
+  }
+  for (; pair < kRopeMaxPairs; ++pair) p->axis[pair] = -1;
+}
+
+bool rope_split_ok(float theta, int32_t d_t, int32_t d_h, int32_t d_w) {
+  if (d_t < 0 || d_h < 0 || d_w < 0 || ((d_t | d_h | d_w) & 1) != 0 || d_t + d_h + d_w > 128) return false;
+  return theta > 0.0f && isfinite(theta);
+}
+}  // namespace
+
 NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, int32_t n_video, int32_t heads,
                                           int32_t head_dim, int64_t row_stride_elems, int32_t frames, int32_t grid_h,
                                           int32_t grid_w, int64_t t0, float theta, int32_t d_t, int32_t d_h,
@@ -218,9 +242,7 @@ NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, i
     return NOMAS_ERR_INVALID_ARG;
   if (head_dim != 128) return NOMAS_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(frames) * grid_h * grid_w != n_video) return NOMAS_ERR_INVALID_ARG;
-  if (d_t < 0 || d_h < 0 || d_w < 0 || ((d_t | d_h | d_w) & 1) != 0 || d_t + d_h + d_w > head_dim)
-    return NOMAS_ERR_INVALID_ARG;
-  if (!(theta > 0.0f) || !isfinite(theta)) return NOMAS_ERR_INVALID_ARG;
+  if (!rope_split_ok(theta, d_t, d_h, d_w)) return NOMAS_ERR_INVALID_ARG;
   if (t0 < 0 || t0 + frames >= (int64_t(1) << 24) || grid_h >= (1 << 24) || grid_w >= (1 << 24))
     return NOMAS_ERR_UNSUPPORTED;
   const int64_t esz = io_dt == NOMAS_BF16 ? 2 : 4;
@@ -229,18 +251,7 @@ NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, i
   if (!aligned16(q) || (k != nullptr && !aligned16(k))) return NOMAS_ERR_INVALID_ARG;
   if (n_video == 0) return NOMAS_OK;
   RopeParams p;
-  memset(&p, 0, sizeof(p));
-  const int dims[3] = {d_t, d_h, d_w};
-  int pair = 0;
-  for (int a = 0; a < 3; ++a) {
-    for (int i = 0; i < dims[a] / 2; ++i, ++pair) {
-      const double f = pow(static_cast<double>(theta), -2.0 * i / dims[a]);
-      p.f_hi[pair] = static_cast<float>(f);
-      p.f_lo[pair] = static_cast<float>(f - static_cast<double>(p.f_hi[pair]));
-      p.axis[pair] = static_cast<int8_t>(a);
-    }
-  }
-  for (; pair < kRopeMaxPairs; ++pair) p.axis[pair] = -1;
+  rope_tables(&p, theta, d_t, d_h, d_w);
   p.n_video = n_video;
   p.heads = heads;
   p.row_stride = row_stride_elems;
@@ -250,8 +261,11 @@ NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, i
   return from_cuda(launch_rope3d(io_dt == NOMAS_BF16, q, k, p, stream));
 }
 
-NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k, const void* v, nomas_dtype in_dt,
-                                            int32_t n_frames, int64_t block_stride_elems, cudaStream_t stream) {
+namespace {
+// Append, optionally with 3D RoPE of the K rows (rope != nullptr: the pair
+// tables; positions are filled in here).
+nomas_status append_impl(nomas_kvcache* cache, const void* k, const void* v, nomas_dtype in_dt, int32_t n_frames,
+                         int64_t block_stride_elems, const RopeParams* rope, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
   if (in_dt != NOMAS_F32 && in_dt != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
@@ -294,12 +308,44 @@ NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k,
       p.err = nullptr;
       sms = 0;
     }
-    st = from_cuda(launch_append(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, sms, stream));
+    if (rope != nullptr) {
+      RopeParams rp = *rope;
+      rp.t0 = cache->total_frames + first;  // absolute latent frame of the first written frame
+      rp.tpf = p.tpf;
+      rp.grid_w = cache->grid_w;
+      rp.heads = cache->heads;
+      rp.n_video = p.n_tokens;
+      rp.row_stride = static_cast<long long>(cache->heads) * cache->head_dim;
+      st = from_cuda(launch_append_rope(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, rp, stream));
+    } else {
+      st = from_cuda(launch_append(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, sms, stream));
+    }
     if (st != NOMAS_OK) return st;
   }
   cache->total_frames = new_total;
   cache->valid_frames = new_valid;
   return NOMAS_OK;
+}
+}  // namespace
+
+NOMAS_API nomas_status nomas_kvcache_append(nomas_kvcache* cache, const void* k, const void* v, nomas_dtype in_dt,
+                                            int32_t n_frames, int64_t block_stride_elems, cudaStream_t stream) {
+  return append_impl(cache, k, v, in_dt, n_frames, block_stride_elems, nullptr, stream);
+}
+
+NOMAS_API nomas_status nomas_kvcache_append_rope(nomas_kvcache* cache, const void* k, const void* v,
+                                                 nomas_dtype in_dt, int32_t n_frames, int64_t block_stride_elems,
+                                                 float theta, int32_t d_t, int32_t d_h, int32_t d_w,
+                                                 cudaStream_t stream) {
+  nomas_status st = validate_cache(cache);
+  if (st != NOMAS_OK) return st;
+  if (!rope_split_ok(theta, d_t, d_h, d_w) || n_frames < 0) return NOMAS_ERR_INVALID_ARG;
+  if (cache->total_frames + n_frames >= (int64_t(1) << 24) || cache->grid_h >= (1 << 24) ||
+      cache->grid_w >= (1 << 24))
+    return NOMAS_ERR_UNSUPPORTED;
+  RopeParams rp;
+  rope_tables(&rp, theta, d_t, d_h, d_w);
+  return append_impl(cache, k, v, in_dt, n_frames, block_stride_elems, &rp, stream);
 }
 
 NOMAS_API size_t nomas_kvcache_archive_frame_bytes(const nomas_kvcache* c) {
@@ -518,15 +564,15 @@ NOMAS_API nomas_status nomas_sparse_select_workspace_bytes(const nomas_kvcache* 
   const int64_t nq = static_cast<int64_t>(n_video) + n_text;
   const int64_t nc = static_cast<int64_t>(cache->valid_frames) * cache->grid_h * cache->grid_w;
   const int64_t n_tiles = (nc + 127) / 128, n_groups = (nq + 511) / 512;
-  *bytes = round256(static_cast<size_t>(cache->heads) * n_tiles * 128 * 4) +
-           round256(static_cast<size_t>(cache->heads) * n_groups * 128 * 4);
+  (void)n_groups;
+  *bytes = round256(static_cast<size_t>(cache->heads) * n_tiles * 128 * 4);
   return NOMAS_OK;
 }
 
 NOMAS_API nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t block, const void* q, int32_t n_video,
                                            int32_t n_text, float keep_fraction, int32_t* tiles, int32_t* counts,
-                                           int32_t max_keep, void* workspace, size_t workspace_bytes,
-                                           cudaStream_t stream) {
+                                           int32_t max_keep, int32_t reuse_key_means, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
   if (block < 0 || block >= cache->num_blocks || n_video < 0 || n_text < 0) return NOMAS_ERR_INVALID_ARG;
@@ -557,15 +603,13 @@ NOMAS_API nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t b
   p.keep = keep;
   p.max_keep = max_keep;
   p.kbar = static_cast<float*>(workspace);
-  p.qbar = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                    round256(static_cast<size_t>(cache->heads) * n_tiles * 128 * 4));
   p.tiles = tiles;
   p.counts = counts;
   if (n_tiles == 0) {
     // Nothing resident: every list is empty.
     return from_cuda(cudaMemsetAsync(counts, 0, static_cast<size_t>(cache->heads) * n_groups * 4, stream));
   }
-  return from_cuda(launch_sparse_select(cache->dtype == NOMAS_INT8, p, stream));
+  return from_cuda(launch_sparse_select(cache->dtype == NOMAS_INT8, reuse_key_means != 0, p, stream));
 }
 
 NOMAS_API nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int32_t block, const void* q,

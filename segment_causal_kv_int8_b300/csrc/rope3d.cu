@@ -8,11 +8,8 @@
 // HBM-bound elementwise kernel: 16 threads own one token, each thread four
 // consecutive pairs (one 16-byte bf16 vector or two float4 of a head row) of a
 // group of heads.  The cos/sin of a (token, pair) is computed once per head
-// group and applied to those heads of Q and K.  The angle pos * f is formed as a two-float product (f = f_hi +
-// f_lo, exact product error by fma) and reduced by the nearest multiple of
-// 2*pi with a three-float 2*pi (Cody-Waite reduction with fma), so the angle
-// error stays ~1e-7 rad at any frame index below 2^24; sincosf then sees |r|
-// <= pi.
+// group and applied to those heads of Q and K (angle arithmetic in
+// rope_math.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -20,35 +17,17 @@
 #include <type_traits>
 
 #include "kernels.h"
+#include "rope_math.cuh"
 
 namespace nomas {
 namespace {
-
-struct TwoPi {
-  float a, b, c;  // 2*pi = a + b + c (each the float nearest the remainder)
-};
-
-__device__ __forceinline__ float reduced_angle(float pos, float f_hi, float f_lo, const TwoPi& tp) {
-  const float a = pos * f_hi;
-  const float a_err = fmaf(pos, f_hi, -a);
-  const float a_lo = fmaf(pos, f_lo, a_err);
-  const float kq = rintf(a * 0.159154943091895336f);
-  float r = fmaf(-kq, tp.a, a);
-  r = fmaf(-kq, tp.b, r);
-  r = fmaf(-kq, tp.c, r);
-  return r + a_lo;
-}
 
 constexpr int kRopeHeadsPerThread = 4;
 
 // Rotate one 8-value group (4 pairs) held as floats.
 __device__ __forceinline__ void rotate8(float (&x)[8], const float (&cs)[4], const float (&sn)[4]) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float x0 = x[2 * e], x1 = x[2 * e + 1];
-    x[2 * e] = fmaf(x0, cs[e], -x1 * sn[e]);
-    x[2 * e + 1] = fmaf(x0, sn[e], x1 * cs[e]);
-  }
+  for (int e = 0; e < 4; ++e) rope_rotate_pair(x[2 * e], x[2 * e + 1], cs[e], sn[e]);
 }
 
 // Block: 16 tokens x 16 lanes (a lane owns 4 consecutive rotary pairs, i.e. 8
@@ -97,7 +76,7 @@ __global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void*
       cs[e] = 1.0f;
       sn[e] = 0.0f;
     } else {
-      sincosf(reduced_angle(pos[a], p.f_hi[pair], p.f_lo[pair], tp), &sn[e], &cs[e]);
+      sincosf(rope_reduced_angle(pos[a], p.f_hi[pair], p.f_lo[pair], tp), &sn[e], &cs[e]);
     }
   }
 #pragma unroll
@@ -139,16 +118,6 @@ __global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void*
   }
 }
 
-TwoPi two_pi_split() {
-  // 2*pi to 64-bit long double precision, split into three floats.
-  const long double tp = 6.283185307179586476925286766559005768L;
-  TwoPi r;
-  r.a = static_cast<float>(tp);
-  r.b = static_cast<float>(tp - static_cast<long double>(r.a));
-  r.c = static_cast<float>(tp - static_cast<long double>(r.a) - static_cast<long double>(r.b));
-  return r;
-}
-
 }  // namespace
 
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream) {
@@ -156,7 +125,7 @@ cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, c
   const dim3 grid(static_cast<unsigned>((p.n_video + 15) / 16),
                   static_cast<unsigned>((p.heads + kRopeHeadsPerThread - 1) / kRopeHeadsPerThread));
   if (grid.y > 65535) return cudaErrorInvalidValue;
-  const TwoPi tp = two_pi_split();
+  const TwoPi tp = rope_two_pi();
   if (bf16_io)
     rope3d_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp);
   else

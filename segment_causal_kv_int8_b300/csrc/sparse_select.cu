@@ -10,8 +10,14 @@
 // highest scores are kept (ties: lower tile first), listed in increasing
 // tile order.
 //
-// Three small kernels: mean key per (head, tile) of the resident cache
-// (dequantised for INT8), mean query per (head, group), and the ranking.
+// Two HBM-bound kernels.  tile_means_kernel reads the resident cache K once
+// (16-byte coalesced loads, int8 codes dequantised with their row scale) and
+// writes the float32 mean key of every (head, tile); the means depend only on
+// the cache, so callers may keep them across the denoising steps of a turn.
+// select_kernel, one CTA per (query group, head), reads the group's queries
+// (a 256-byte row slice per query, eight loads in flight per thread), scores
+// every tile, ranks the scores and writes the kept list with a block-wide
+// prefix count.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -21,86 +27,210 @@
 namespace nomas {
 namespace {
 
-// One CTA per (tile, head); thread d sums dimension d over the tile's rows.
+constexpr int kSelThreads = 256;
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& w) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc[2 * e] += __uint_as_float(v[e] << 16);
+    acc[2 * e + 1] += __uint_as_float(v[e] & 0xFFFF0000u);
+  }
+}
+
+// One CTA per (tile, head).  BF16: 16 lanes cover a 256-byte key row, so the
+// 256 threads take 16 rows at a time (8 passes for a full tile).  INT8: 8
+// lanes cover a 128-byte row, 32 rows at a time (4 passes); each code is
+// multiplied by its row scale before it is summed.  Partial sums (one per
+// row lane) are added in a fixed order in shared memory.
 template <bool kInt8>
-__global__ void __launch_bounds__(128) tile_means_kernel(const SparseSelectParams p) {
-  const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+__global__ void __launch_bounds__(kSelThreads) tile_means_kernel(const SparseSelectParams p) {
+  constexpr int kLanesPerRow = kInt8 ? 8 : 16;    // 16-byte vectors per row
+  constexpr int kDims = 128 / kLanesPerRow;       // dims per thread
+  constexpr int kRowSlots = kSelThreads / kLanesPerRow;
+  __shared__ float part[kRowSlots][129];
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int c = threadIdx.x % kLanesPerRow, rs = threadIdx.x / kLanesPerRow;
   const long long plane = static_cast<long long>(p.block_head_base + h) * p.cap_slots;
-  const int r0 = t * 128, r1 = min(p.nc, r0 + 128);
-  float acc = 0.0f;
-  for (int r = r0; r < r1; ++r) {
-    float x;
-    if constexpr (kInt8) {
-      x = static_cast<float>(static_cast<const int8_t*>(p.kcache)[(plane + r) * 128 + d]) * p.kscale[plane + r];
-    } else {
-      x = __bfloat162float(static_cast<const __nv_bfloat16*>(p.kcache)[(plane + r) * 128 + d]);
+  const int r0 = t * 128, n = min(128, p.nc - r0);
+  float acc[kDims];
+#pragma unroll
+  for (int e = 0; e < kDims; ++e) acc[e] = 0.0f;
+#pragma unroll
+  for (int pass = 0; pass < 128 / kRowSlots; ++pass) {
+    const int r = pass * kRowSlots + rs;
+    if (r < n) {
+      const long long row = plane + r0 + r;
+      if constexpr (kInt8) {
+        const uint4 w = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(p.kcache) + row * 128)[c];
+        const float s = p.kscale[row];
+        const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int8_t code = static_cast<int8_t>((v[e >> 2] >> (8 * (e & 3))) & 0xFFu);
+          acc[e] += static_cast<float>(code) * s;
+        }
+      } else {
+        const uint4 w = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.kcache) + row * 128)[c];
+        add_bf16x8(acc, w);
+      }
     }
-    acc += x;
   }
-  p.kbar[(static_cast<size_t>(h) * p.n_tiles + t) * 128 + d] = acc / static_cast<float>(r1 - r0);
+#pragma unroll
+  for (int e = 0; e < kDims; ++e) part[rs][c * kDims + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    float s = 0.0f;
+    for (int i = 0; i < kRowSlots; ++i) s += part[i][threadIdx.x];
+    p.kbar[(static_cast<size_t>(h) * p.n_tiles + t) * 128 + threadIdx.x] = s / static_cast<float>(n);
+  }
 }
 
-// One CTA per (group, head): mean of the group's query rows.
-__global__ void __launch_bounds__(128) group_means_kernel(const SparseSelectParams p) {
-  const int g = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-  const int r0 = g * 512, r1 = min(p.nq, r0 + 512);
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  float acc = 0.0f;
-  for (int r = r0; r < r1; ++r) acc += __bfloat162float(q[(static_cast<size_t>(r) * p.heads + h) * 128 + d]);
-  p.qbar[(static_cast<size_t>(h) * p.n_groups + g) * 128 + d] = acc / static_cast<float>(r1 - r0);
-}
+// One CTA of 512 threads per (query group, head).
+constexpr int kPickThreads = 512;
 
-// One CTA per (group, head): scores of every tile, rank (score descending,
-// index ascending), keep ranks below k, write them in increasing order.
-__global__ void __launch_bounds__(256) rank_kernel(const SparseSelectParams p) {
-  extern __shared__ float s_scores[];  // [n_tiles]
+__global__ void __launch_bounds__(kPickThreads, 2) select_kernel(const SparseSelectParams p) {
+  // Dynamic shared memory: first the partial query sums [32][129], later
+  // (after a barrier) the scores [n4 * 4] (padded with -inf) followed by keep
+  // flags [n_tiles].
+  extern __shared__ float s_dyn[];
+  float(*part)[129] = reinterpret_cast<float(*)[129]>(s_dyn);
+  float* s_scores = s_dyn;
   __shared__ float s_q[128];
+  __shared__ int s_warp[kPickThreads / 32];
   const int g = blockIdx.x, h = blockIdx.y;
-  if (threadIdx.x < 128) s_q[threadIdx.x] = p.qbar[(static_cast<size_t>(h) * p.n_groups + g) * 128 + threadIdx.x];
-  __syncthreads();
-  for (int t = threadIdx.x; t < p.n_tiles; t += blockDim.x) {
-    const float* kb = p.kbar + (static_cast<size_t>(h) * p.n_tiles + t) * 128;
-    float acc = 0.0f;
-    for (int d = 0; d < 128; ++d) acc = fmaf(s_q[d], kb[d], acc);
-    s_scores[t] = acc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Mean query of the group: 16 lanes per 256-byte row slice, 32 rows a
+  // pass; the loads of eight passes are in flight before any is summed.
+  {
+    const int c = threadIdx.x & 15, rs = threadIdx.x >> 4;
+    const int r0 = g * 512, n = min(512, p.nq - r0);
+    const uint4* q = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q)) +
+                     (static_cast<size_t>(r0) * p.heads + h) * 16 + c;
+    const size_t row_vecs = static_cast<size_t>(p.heads) * 16;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      uint4 w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rs + 32 * (8 * half + i);
+        w[i] = r < n ? q[r * row_vecs] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) add_bf16x8(acc, w[i]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[rs][c * 8 + e] = acc[e];
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      float s = 0.0f;
+      for (int i = 0; i < 32; ++i) s += part[i][threadIdx.x];
+      s_q[threadIdx.x] = s / static_cast<float>(n);
+    }
+    __syncthreads();
   }
+
+  // Scores: four lanes per tile, each a quarter of the dot product (eight
+  // float4 loads of the tile's mean key), summed by shuffles.
+  for (int t0 = 0; t0 < p.n_tiles; t0 += kPickThreads / 4) {
+    const int t = t0 + (threadIdx.x >> 2), qd = threadIdx.x & 3;
+    float a = 0.0f;
+    if (t < p.n_tiles) {
+      const float4* kb =
+          reinterpret_cast<const float4*>(p.kbar + (static_cast<size_t>(h) * p.n_tiles + t) * 128 + 32 * qd);
+      const float* sq = s_q + 32 * qd;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        float4 k4[4];
+#pragma unroll
+        for (int d = 0; d < 4; ++d) k4[d] = kb[4 * hb + d];
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+          const float* sqd = sq + 16 * hb + 4 * d;
+          a = fmaf(sqd[0], k4[d].x, a);
+          a = fmaf(sqd[1], k4[d].y, a);
+          a = fmaf(sqd[2], k4[d].z, a);
+          a = fmaf(sqd[3], k4[d].w, a);
+        }
+      }
+    }
+    a += __shfl_xor_sync(0xffffffffu, a, 1);
+    a += __shfl_xor_sync(0xffffffffu, a, 2);
+    if (t < p.n_tiles && qd == 0) s_scores[t] = a;
+  }
+  const int n4 = (p.n_tiles + 3) >> 2;
+  if (threadIdx.x < 4 * n4 - p.n_tiles) s_scores[p.n_tiles + threadIdx.x] = -INFINITY;
   __syncthreads();
-  unsigned char* keep = reinterpret_cast<unsigned char*>(s_scores + p.n_tiles);
-  for (int t = threadIdx.x; t < p.n_tiles; t += blockDim.x) {
+
+  // Rank = tiles with a higher score, or an equal score and a lower index:
+  // tiles before t count when su >= st, tiles after t when su > st (the -inf
+  // padding never counts).  Four scores per shared-memory load.
+  unsigned char* keep = reinterpret_cast<unsigned char*>(s_scores + 4 * n4);
+  const float4* s4 = reinterpret_cast<const float4*>(s_scores);
+  for (int t = threadIdx.x; t < p.n_tiles; t += kPickThreads) {
     const float st = s_scores[t];
+    const int tc = t >> 2;
     int rank = 0;
-    for (int u = 0; u < p.n_tiles; ++u) {
+    for (int u4 = 0; u4 < tc; ++u4) {
+      const float4 v = s4[u4];
+      rank += (v.x >= st) + (v.y >= st) + (v.z >= st) + (v.w >= st);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int u = 4 * tc + e;
       const float su = s_scores[u];
-      rank += (su > st || (su == st && u < t)) ? 1 : 0;
+      rank += u < t ? (su >= st) : (u > t ? (su > st) : 0);
+    }
+    for (int u4 = tc + 1; u4 < n4; ++u4) {
+      const float4 v = s4[u4];
+      rank += (v.x > st) + (v.y > st) + (v.z > st) + (v.w > st);
     }
     keep[t] = rank < p.keep ? 1 : 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const size_t hg = static_cast<size_t>(h) * p.n_groups + g;
-    int* out = p.tiles + hg * p.max_keep;
-    int c = 0;
-    for (int t = 0; t < p.n_tiles && c < p.keep; ++t)
-      if (keep[t]) out[c++] = t;
-    p.counts[hg] = c;
+
+  // Kept tiles in increasing order: position = kept tiles before this one.
+  const size_t hg = static_cast<size_t>(h) * p.n_groups + g;
+  int* out = p.tiles + hg * p.max_keep;
+  int base = 0;
+  for (int t0 = 0; t0 < p.n_tiles; t0 += kPickThreads) {
+    const int t = t0 + threadIdx.x;
+    const bool k = t < p.n_tiles && keep[t];
+    const unsigned bal = __ballot_sync(0xffffffffu, k);
+    if (lane == 0) s_warp[warp] = __popc(bal);
+    __syncthreads();
+    int before = base;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    before += __popc(bal & ((1u << lane) - 1u));
+    if (k && before < p.keep) out[before] = t;
+    for (int w = 0; w < kPickThreads / 32; ++w) base += s_warp[w];
+    __syncthreads();
   }
+  if (threadIdx.x == 0) p.counts[hg] = min(base, p.keep);
 }
 
 }  // namespace
 
-size_t sparse_select_smem(int n_tiles) { return static_cast<size_t>(n_tiles) * 5; }
+size_t sparse_select_smem(int n_tiles) {
+  const size_t need = static_cast<size_t>((n_tiles + 3) & ~3) * 4 + n_tiles, part = 32 * 129 * sizeof(float);
+  return ((need > part ? need : part) + 15) & ~size_t(15);
+}
 
-cudaError_t launch_sparse_select(bool int8_cache, const SparseSelectParams& p, cudaStream_t stream) {
-  if (p.n_tiles > 0) {
+cudaError_t launch_sparse_select(bool int8_cache, bool reuse_key_means, const SparseSelectParams& p,
+                                 cudaStream_t stream) {
+  if (p.n_tiles > 0 && !reuse_key_means) {
     const dim3 tg(p.n_tiles, p.heads);
     if (int8_cache)
-      tile_means_kernel<true><<<tg, 128, 0, stream>>>(p);
+      tile_means_kernel<true><<<tg, kSelThreads, 0, stream>>>(p);
     else
-      tile_means_kernel<false><<<tg, 128, 0, stream>>>(p);
+      tile_means_kernel<false><<<tg, kSelThreads, 0, stream>>>(p);
   }
   const dim3 gg(p.n_groups, p.heads);
-  group_means_kernel<<<gg, 128, 0, stream>>>(p);
-  if (p.n_tiles > 0) rank_kernel<<<gg, 256, sparse_select_smem(p.n_tiles), stream>>>(p);
+  select_kernel<<<gg, kPickThreads, sparse_select_smem(p.n_tiles), stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -159,26 +159,26 @@ def test_sparse_entry_points_validate_before_launching():
     d = _desc(heads=2, gh=23, gw=40, cap=18, past=18, total=24, valid=18)
     out = ctypes.c_size_t()
     assert nomas.nomas_sparse_select_workspace_bytes(ctypes.byref(d), 7360, 256, out) == nomas.NOMAS_OK
-    n_tiles, groups = 130, 15
-    assert out.value == -(-2 * n_tiles * 512 // 256) * 256 + -(-2 * groups * 512 // 256) * 256
+    n_tiles = 130
+    assert out.value == -(-2 * n_tiles * 512 // 256) * 256
     k = nomas.sparse_keep_count(n_tiles, 0.25)
     assert k == 33  # ceil(32.5)
     ws = 1 << 20
     # keep fraction outside (0, 1]
     for keep in (0.0, -0.5, 1.5, float("nan")):
-        assert nomas.nomas_sparse_select(ctypes.byref(d), 0, 256, 7360, 256, keep, 256, 256, k, ws, out.value,
-                                         None) == nomas.NOMAS_ERR_INVALID_ARG
+        assert nomas.nomas_sparse_select(ctypes.byref(d), 0, 256, 7360, 256, keep, 256, 256, k, 0, ws,
+                                         out.value, None) == nomas.NOMAS_ERR_INVALID_ARG
     # rows shorter than the kept count, missing workspace, block out of range
-    assert nomas.nomas_sparse_select(ctypes.byref(d), 0, 256, 7360, 256, 0.25, 256, 256, k - 1, ws, out.value,
-                                     None) == nomas.NOMAS_ERR_INVALID_ARG
-    assert nomas.nomas_sparse_select(ctypes.byref(d), 0, 256, 7360, 256, 0.25, 256, 256, k, None, 0,
-                                     None) == nomas.NOMAS_ERR_INVALID_ARG
-    assert nomas.nomas_sparse_select(ctypes.byref(d), 1, 256, 7360, 256, 0.25, 256, 256, k, ws, out.value,
-                                     None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert nomas.nomas_sparse_select(ctypes.byref(d), 0, 256, 7360, 256, 0.25, 256, 256, k - 1, 0, ws,
+                                     out.value, None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert nomas.nomas_sparse_select(ctypes.byref(d), 0, 256, 7360, 256, 0.25, 256, 256, k, 0, None,
+                                     0, None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert nomas.nomas_sparse_select(ctypes.byref(d), 1, 256, 7360, 256, 0.25, 256, 256, k, 0, ws,
+                                     out.value, None) == nomas.NOMAS_ERR_INVALID_ARG
     # more than 8192 resident tiles
     big = _desc(heads=2, gh=128, gw=128, cap=70, total=70, valid=70)
-    assert nomas.nomas_sparse_select(ctypes.byref(big), 0, 256, 128, 0, 0.25, 256, 256, 9000, ws, 1 << 30,
-                                     None) == nomas.NOMAS_ERR_UNSUPPORTED
+    assert nomas.nomas_sparse_select(ctypes.byref(big), 0, 256, 128, 0, 0.25, 256, 256, 9000, 0, ws,
+                                     1 << 30, None) == nomas.NOMAS_ERR_UNSUPPORTED
     # sparse attention without lists
     assert nomas.nomas_segment_attn_sparse(ctypes.byref(d), 0, 256, 256, 256, 7360, 256, 0.1, None, 256, k, 256,
                                            None, None, 0, 0, None) == nomas.NOMAS_ERR_INVALID_ARG

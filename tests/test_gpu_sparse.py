@@ -237,3 +237,18 @@ def test_out_of_range_entry_is_reported_and_contained():
     torch.cuda.synchronize()
     assert nomas.device_error(clear=True) == nomas.NOMAS_ERR_INVALID_ARG
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_reused_key_means_give_the_same_lists():
+    # the mean keys of an unchanged cache serve every step of a turn
+    wl = _variant(2)
+    gc, _ = build_caches(wl)
+    n_t = -(-gc.valid_frames * gc.tpf // 128)
+    ws = torch.empty(max(256, n_t * wl.heads * 512), dtype=torch.uint8, device="cuda")
+    for step in range(3):
+        q, _, _ = current_qkv(wl, step=step)
+        qd = to_dev(q, "bf16")
+        fresh = nomas.sparse_select(gc, 0, qd, wl.n_video, wl.n_text, 0.25)
+        reused = nomas.sparse_select(gc, 0, qd, wl.n_video, wl.n_text, 0.25, workspace=ws,
+                                     reuse_key_means=step > 0)
+        assert torch.equal(fresh[0], reused[0]) and torch.equal(fresh[1], reused[1])
