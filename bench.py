@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
+    ap.add_argument("--append-rope", action="store_true",
+                    help="write the history with the fused RoPE + append (keys rotated on the way into the cache)")
     ap.add_argument("--sparse", type=float, default=0.0,
                     help="block-sparse attention keeping this fraction of cache tiles (0 = dense)")
     ap.add_argument("--archive", action="store_true",
@@ -292,7 +294,10 @@ def run_ours(args):
         if ev is not None:
             ev[0].record(stream)
         for kh, vh in hist_d:
-            cache.append(kh, vh)
+            if args.append_rope:
+                cache.append_rope(kh, vh, wl.theta, wl.rope_split)
+            else:
+                cache.append(kh, vh)
         if ev is not None:
             ev[1].record(stream)
             ev[2].record(stream)
@@ -365,7 +370,7 @@ def run_ours(args):
     achieved = flops / (attn_avg * 1e-3) / 1e12
 
     e2e = None
-    if not args.no_e2e and not keep:
+    if not args.no_e2e and not keep and not args.append_rope:
         e2e = _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world)
 
     launches_per_step = len(hist) + 1 + 1 + (1 if splits_used > 1 else 0) + (3 if keep and wl.n_cache else 0)
@@ -377,12 +382,13 @@ def run_ours(args):
     row_bytes = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if wl.cache_dtype == "int8" else 2 * wl.head_dim))
     append_bytes = sum(min(f, wl.window) for f in wl.cache_frames_hist) * wl.tpf * wl.heads * row_bytes
     elementwise = {}
-    for name, nbytes, ms in (("kvcache_append", append_bytes, append_ms), ("rope3d", rope_bytes, rope_ms)):
+    append_name = "kvcache_append_rope" if args.append_rope else "kvcache_append"
+    for name, nbytes, ms in ((append_name, append_bytes, append_ms), ("rope3d", rope_bytes, rope_ms)):
         t = statistics.mean(ms)
         gbs = nbytes / (t * 1e-3) / 1e9 if t > 0 else None
         elementwise[name] = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": 1e3 * t, "achieved": gbs,
                              "peak": hbm, "unit": "GB/s", "frac": gbs / hbm if gbs else None,
-                             "launches_per_step": len(hist) if name == "kvcache_append" else 1}
+                             "launches_per_step": len(hist) if name == append_name else 1}
     traffic = _load_traffic(args.config)
     if rank == 0:
         line = {
@@ -400,6 +406,8 @@ def run_ours(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if args.append_rope:
+            line["config"]["workload"] += "; history written by the fused RoPE + append"
         if keep:
             # Executed FLOPs count each query group's kept keys; the dense
             # equivalent is the full-attention FLOPs over the same step time.
