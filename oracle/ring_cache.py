@@ -26,14 +26,16 @@ Reading used here (the plainest the rest supports):
   ``[0, valid_frames * tpf)`` (the ring fills from slot 0);
 * without a window, appending past the capacity is an error.
 
-INT8 caches store codes and per-row scales from :mod:`oracle.int8_codec`; BF16
+INT8 caches store codes and per-row scales from :mod:`oracle.int8_codec`, FP8
+caches (the comparison format) E4M3 codes and scales from
+:mod:`oracle.fp8_codec`; BF16
 caches store the values rounded to bf16 (round to nearest even).
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import int8_codec
+from . import fp8_codec, int8_codec
 from .rope3d import rope3d_segment
 
 
@@ -58,8 +60,8 @@ class RingCache:
             raise ValueError("bad capacity / window")
         if past_frames > 0 and capacity_frames != past_frames:
             raise ValueError("a windowed cache must have capacity_frames == past_frames")
-        if dtype not in ("int8", "bf16"):
-            raise ValueError("dtype must be 'int8' or 'bf16'")
+        if dtype not in ("int8", "fp8", "bf16"):
+            raise ValueError("dtype must be 'int8', 'fp8' or 'bf16'")
         self.blocks, self.heads, self.head_dim = blocks, heads, head_dim
         self.grid_h, self.grid_w = grid_h, grid_w
         self.tpf = grid_h * grid_w
@@ -71,9 +73,9 @@ class RingCache:
         self.store = store
         if store:
             shape = (blocks, heads, self.slots, head_dim)
-            if dtype == "int8":
-                self.k_codes = np.zeros(shape, np.int8)
-                self.v_codes = np.zeros(shape, np.int8)
+            if dtype in ("int8", "fp8"):
+                self.k_codes = np.zeros(shape, np.int8 if dtype == "int8" else np.uint8)
+                self.v_codes = np.zeros(shape, np.int8 if dtype == "int8" else np.uint8)
                 self.k_scales = np.zeros(shape[:3], np.float32)
                 self.v_scales = np.zeros(shape[:3], np.float32)
             else:
@@ -122,9 +124,10 @@ class RingCache:
                 dst = slice(sf * self.tpf, (sf + 1) * self.tpf)
                 kk = np.transpose(k[:, rows], (0, 2, 1, 3))        # [blocks][heads][tpf][D]
                 vv = np.transpose(v[:, rows], (0, 2, 1, 3))
-                if self.dtype == "int8":
-                    self.k_codes[:, :, dst], self.k_scales[:, :, dst] = int8_codec.quantize_rows(kk)
-                    self.v_codes[:, :, dst], self.v_scales[:, :, dst] = int8_codec.quantize_rows(vv)
+                if self.dtype in ("int8", "fp8"):
+                    codec = int8_codec if self.dtype == "int8" else fp8_codec
+                    self.k_codes[:, :, dst], self.k_scales[:, :, dst] = codec.quantize_rows(kk)
+                    self.v_codes[:, :, dst], self.v_scales[:, :, dst] = codec.quantize_rows(vv)
                 else:
                     self.k_vals[:, :, dst] = _bf16_round(kk)
                     self.v_vals[:, :, dst] = _bf16_round(vv)
@@ -172,9 +175,10 @@ class RingCache:
         Returns float64 ``[n_resident_tokens][heads][D]`` each, in slot order.
         """
         n = self.n_resident_tokens()
-        if self.dtype == "int8":
-            k = int8_codec.dequantize_rows(self.k_codes[block, :, :n], self.k_scales[block, :, :n])
-            v = int8_codec.dequantize_rows(self.v_codes[block, :, :n], self.v_scales[block, :, :n])
+        if self.dtype in ("int8", "fp8"):
+            codec = int8_codec if self.dtype == "int8" else fp8_codec
+            k = codec.dequantize_rows(self.k_codes[block, :, :n], self.k_scales[block, :, :n])
+            v = codec.dequantize_rows(self.v_codes[block, :, :n], self.v_scales[block, :, :n])
         else:
             k = self.k_vals[block, :, :n]
             v = self.v_vals[block, :, :n]
@@ -193,6 +197,6 @@ class RingCache:
     def bytes(self) -> int:
         """Device bytes of the cache storage (K and V, codes or bf16, plus scales)."""
         per = self.blocks * self.heads * self.slots
-        if self.dtype == "int8":
+        if self.dtype in ("int8", "fp8"):
             return 2 * per * (self.head_dim + 4)
         return 2 * per * self.head_dim * 2
