@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
+    ap.add_argument("--cache-dtype", choices=["int8", "fp8", "bf16"], default=None,
+                    help="override the config's cache format (fp8: the E4M3 comparison variant)")
     ap.add_argument("--append-rope", action="store_true",
                     help="write the history with the fused RoPE + append (keys rotated on the way into the cache)")
     ap.add_argument("--sparse", type=float, default=0.0,
@@ -246,6 +248,9 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     wl = CONFIGS[args.config]
+    if args.cache_dtype:
+        import dataclasses
+        wl = dataclasses.replace(wl, cache_dtype=args.cache_dtype)
     block = rank_block(rank)  # each rank owns an independent block's data
 
     # ---- synthetic inputs (seeded), resident in HBM before timing
@@ -379,7 +384,7 @@ def run_ours(args):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     in_esz = 2 if wl.io_dtype == "bf16" else 4
     rope_bytes = wl.n_video * wl.heads * wl.head_dim * in_esz * 2 * 2  # Q and K, read + write
-    row_bytes = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if wl.cache_dtype == "int8" else 2 * wl.head_dim))
+    row_bytes = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if wl.cache_dtype in ("int8", "fp8") else 2 * wl.head_dim))
     append_bytes = sum(min(f, wl.window) for f in wl.cache_frames_hist) * wl.tpf * wl.heads * row_bytes
     elementwise = {}
     append_name = "kvcache_append_rope" if args.append_rope else "kvcache_append"
@@ -389,7 +394,8 @@ def run_ours(args):
         elementwise[name] = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": 1e3 * t, "achieved": gbs,
                              "peak": hbm, "unit": "GB/s", "frac": gbs / hbm if gbs else None,
                              "launches_per_step": len(hist) if name == append_name else 1}
-    traffic = _load_traffic(args.config)
+    # the committed counters describe the config's own cache format
+    traffic = _load_traffic(args.config) if wl.cache_dtype == CONFIGS[args.config].cache_dtype else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -49,7 +49,7 @@ typedef enum {
   NOMAS_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up waiting on an on-chip barrier   */
 } nomas_status;
 
-typedef enum { NOMAS_F32 = 0, NOMAS_BF16 = 1, NOMAS_INT8 = 2 } nomas_dtype;
+typedef enum { NOMAS_F32 = 0, NOMAS_BF16 = 1, NOMAS_INT8 = 2, NOMAS_FP8 = 3 } nomas_dtype;
 
 /*
  * Persistent KV cache of num_blocks transformer blocks (the lifelong cache of
@@ -58,7 +58,8 @@ typedef enum { NOMAS_F32 = 0, NOMAS_BF16 = 1, NOMAS_INT8 = 2 } nomas_dtype;
  *
  * Layout (caller-allocated device memory):
  *   k, v       [num_blocks][heads][capacity_frames * grid_h * grid_w][head_dim]
- *              int8 codes (dtype NOMAS_INT8) or bf16 values (NOMAS_BF16)
+ *              int8 codes (dtype NOMAS_INT8), E4M3 codes (NOMAS_FP8) or bf16
+ *              values (NOMAS_BF16)
  *   k_scale,   [num_blocks][heads][capacity_frames * grid_h * grid_w] float32,
  *   v_scale    one scale per (block, head, token); NULL for NOMAS_BF16
  * Absolute latent frame f lives in frame-slot (f mod capacity_frames); token
@@ -66,6 +67,12 @@ typedef enum { NOMAS_F32 = 0, NOMAS_BF16 = 1, NOMAS_INT8 = 2 } nomas_dtype;
  * h*grid_w + w.  Resident slots are always [0, valid_frames*grid_h*grid_w).
  * INT8 codes: scale = fl32(absmax/127), code = clamp(rint(fl32(x *
  * fl32(127/absmax))), -127, 127), ties to even; an all-zero row has scale 0.
+ * FP8 codes (a comparison format beside the pages' INT8): OCP E4M3 bytes,
+ * scale = fl32(absmax/448), code = E4M3(fl32(x * fl32(448/absmax))), nearest
+ * with ties to the even code, saturating at +-448; a NaN product (0 * inf,
+ * only for a zero or tiny row) is coded 0.  Every call accepts a NOMAS_FP8
+ * cache wherever it accepts NOMAS_INT8 (the archive included); the attention
+ * dequantises value(code) * scale to bf16 in shared memory.
  *
  * past_frames > 0 is a sliding window of that many latent frames and requires
  * capacity_frames == past_frames; past_frames == 0 means no window (appending
@@ -82,11 +89,11 @@ typedef struct {
   int32_t grid_w;          /* latent columns per frame                            */
   int32_t capacity_frames; /* ring size in latent frames                          */
   int32_t past_frames;     /* window in latent frames; 0 = none                   */
-  int32_t dtype;           /* nomas_dtype: NOMAS_INT8 or NOMAS_BF16               */
+  int32_t dtype;           /* nomas_dtype: NOMAS_INT8, NOMAS_FP8 or NOMAS_BF16    */
   void* k;                 /* device                                              */
   void* v;                 /* device                                              */
-  float* k_scale;          /* device, INT8 only                                   */
-  float* v_scale;          /* device, INT8 only                                   */
+  float* k_scale;          /* device, INT8 / FP8 only                             */
+  float* v_scale;          /* device, INT8 / FP8 only                             */
   int64_t total_frames;    /* absolute latent frames ever appended (host)         */
   int32_t valid_frames;    /* resident frames = min(total_frames, window) (host)  */
   int32_t reserved;        /* must be 0                                           */

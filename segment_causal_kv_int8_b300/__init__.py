@@ -39,6 +39,7 @@ NOMAS_ERR_DEVICE_TIMEOUT = 5
 NOMAS_F32 = 0
 NOMAS_BF16 = 1
 NOMAS_INT8 = 2
+NOMAS_FP8 = 3
 
 
 class nomas_kvcache(ctypes.Structure):
@@ -160,7 +161,8 @@ def rope3d(q, k, frames: int, grid_h: int, grid_w: int, t0: int, theta: float = 
 class KVCache:
     """A persistent ring KV cache whose device buffers are torch tensors.
 
-    ``dtype``: "int8" (codes + float32 per-(block, head, token) scales) or "bf16".
+    ``dtype``: "int8" (codes + float32 per-(block, head, token) scales), "fp8" (E4M3 codes
+    as uint8 + scales; the comparison format) or "bf16".
     """
 
     def __init__(self, num_blocks: int, heads: int, grid_h: int, grid_w: int, capacity_frames: int,
@@ -168,19 +170,20 @@ class KVCache:
         torch = _torch()
         slots = capacity_frames * grid_h * grid_w
         shape = (num_blocks, heads, slots, head_dim)
-        if dtype == "int8":
-            self.k = torch.zeros(shape, dtype=torch.int8, device=device)
-            self.v = torch.zeros(shape, dtype=torch.int8, device=device)
+        if dtype in ("int8", "fp8"):
+            code_t = torch.int8 if dtype == "int8" else torch.uint8
+            self.k = torch.zeros(shape, dtype=code_t, device=device)
+            self.v = torch.zeros(shape, dtype=code_t, device=device)
             self.k_scale = torch.zeros(shape[:3], dtype=torch.float32, device=device)
             self.v_scale = torch.zeros(shape[:3], dtype=torch.float32, device=device)
-            code = NOMAS_INT8
+            code = NOMAS_INT8 if dtype == "int8" else NOMAS_FP8
         elif dtype == "bf16":
             self.k = torch.zeros(shape, dtype=torch.bfloat16, device=device)
             self.v = torch.zeros(shape, dtype=torch.bfloat16, device=device)
             self.k_scale = self.v_scale = None
             code = NOMAS_BF16
         else:
-            raise ValueError("dtype must be 'int8' or 'bf16'")
+            raise ValueError("dtype must be 'int8', 'fp8' or 'bf16'")
         self.dtype = dtype
         self.desc = nomas_kvcache(num_blocks, heads, head_dim, grid_h, grid_w, capacity_frames, past_frames, code,
                                   self.k.data_ptr(), self.v.data_ptr(),

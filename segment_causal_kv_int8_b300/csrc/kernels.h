@@ -9,6 +9,12 @@
 namespace nomas {
 
 // ------------------------------------------------------------------ RoPE-3D
+// Cache storage kinds: bf16 values, or one-byte codes (INT8 or FP8 E4M3)
+// with one float32 scale per (block, head, token).
+constexpr int kCacheBF16 = 0;
+constexpr int kCacheInt8 = 1;
+constexpr int kCacheFp8 = 2;
+
 constexpr int kRopeMaxPairs = 64;  // head_dim 128 -> 64 rotary pairs
 
 struct RopeParams {
@@ -46,10 +52,10 @@ struct AppendParams {
   uint32_t* err;                 // device error word (staged kernel's bounded waits)
 };
 
-cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p, int sms, cudaStream_t stream);
+cudaError_t launch_append(bool f32_in, int kind, const AppendParams& p, int sms, cudaStream_t stream);
 // Append with 3D RoPE of the K rows (rp.t0 = absolute frame of the first
 // written frame; rp.tpf, rp.grid_w and the pair tables set).
-cudaError_t launch_append_rope(bool f32_in, bool int8_cache, const AppendParams& p, const RopeParams& rp,
+cudaError_t launch_append_rope(bool f32_in, int kind, const AppendParams& p, const RopeParams& rp,
                                cudaStream_t stream);
 
 // ------------------------------------------------------------------ reset
@@ -78,7 +84,7 @@ struct SparseSelectParams {
 };
 
 size_t sparse_select_smem(int n_tiles);
-cudaError_t launch_sparse_select(bool int8_cache, bool reuse_key_means, const SparseSelectParams& p,
+cudaError_t launch_sparse_select(int kind, bool reuse_key_means, const SparseSelectParams& p,
                                  cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention
@@ -109,7 +115,7 @@ struct AttnParams {
   int n_groups;                  // 512-query groups (two 256-query blocks each)
 };
 
-cudaError_t launch_segment_attn(bool int8_cache, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
+cudaError_t launch_segment_attn(int kind, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
                                 cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
 int attn_smem_bytes(bool int8_cache);

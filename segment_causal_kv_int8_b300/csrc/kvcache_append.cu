@@ -21,6 +21,7 @@
 // +-inf or NaN (0 * inf): that row takes a float->int conversion instead,
 // with NaN -> 0 and +-inf clamped to +-127.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,21 +50,48 @@ __device__ __forceinline__ void load8(const void* base, long long off, float (&x
   }
 }
 
+// E4M3 codes of fl32(x[i] * inv), four per word with x[4q] in the low byte.
+// The conversion rounds to nearest (ties to even) and saturates at +-448; when
+// inv overflowed (finite_inv false) a NaN product (0 * inf) is coded 0.
+template <int N>
+__device__ __forceinline__ void fp8_encode(const float (&x)[N], float inv, bool finite_inv, uint32_t (&out)[N / 4]) {
+#pragma unroll
+  for (int q = 0; q < N / 4; ++q) {
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = __fmul_rn(x[4 * q + e], inv);
+    if (!finite_inv) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (isnan(y[e])) y[e] = 0.0f;
+    }
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y[0], y[1]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y[2], y[3]), __NV_SATFINITE, __NV_E4M3);
+    out[q] = (lo & 0xFFFFu) | (hi << 16);
+  }
+}
+
 // Quantise (or copy) one row from 8 values per lane of a 16-lane group and
-// write it to its ring slot.
-template <bool kInt8>
+// write it to its ring slot.  K: kCacheBF16, kCacheInt8 or kCacheFp8.
+template <int K>
 __device__ __forceinline__ void write_row(const AppendParams& p, int tensor, long long dst_row, const float (&x)[8],
                                           int g, unsigned gmask) {
-  if constexpr (kInt8) {
+  if constexpr (K != kCacheBF16) {
+    constexpr float kQMax = K == kCacheInt8 ? 127.0f : 448.0f;
     float m = 0.0f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
-    const float scale = __fdiv_rn(m, 127.0f);
-    const float inv = __fdiv_rn(127.0f, m);
+    const float scale = __fdiv_rn(m, kQMax);
+    const float inv = __fdiv_rn(kQMax, m);
     uint32_t lo, hi;
-    if (inv <= 3.0e38f) {
+    if constexpr (K == kCacheFp8) {
+      uint32_t c[2];
+      fp8_encode<8>(x, inv, inv <= 3.0e38f, c);
+      lo = c[0];
+      hi = c[1];
+    } else if (inv <= 3.0e38f) {
       // |fl32(x * inv)| <= 127: adding 1.5 * 2^23 rounds it to an integer
       // (nearest, ties to even) held in the low mantissa bits, whose low byte
       // is the two's-complement code.
@@ -106,10 +134,11 @@ __device__ __forceinline__ void write_row(const AppendParams& p, int tensor, lon
 
 // Quantise (or round to bf16) one row from 16 values per lane of an 8-lane
 // group and write it to its ring slot.
-template <bool kInt8>
+template <int K>
 __device__ __forceinline__ void store_row16(const AppendParams& p, int tensor, long long dst_row, const float (&x)[16],
                                             int g, unsigned gmask) {
-  if constexpr (kInt8) {
+  if constexpr (K != kCacheBF16) {
+    constexpr float kQMax = K == kCacheInt8 ? 127.0f : 448.0f;
     float m0 = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
     float m1 = fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7])));
     float m2 = fmaxf(fmaxf(fabsf(x[8]), fabsf(x[9])), fmaxf(fabsf(x[10]), fabsf(x[11])));
@@ -117,10 +146,12 @@ __device__ __forceinline__ void store_row16(const AppendParams& p, int tensor, l
     float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 #pragma unroll
     for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, off));
-    const float scale = __fdiv_rn(m, 127.0f);
-    const float inv = __fdiv_rn(127.0f, m);
+    const float scale = __fdiv_rn(m, kQMax);
+    const float inv = __fdiv_rn(kQMax, m);
     uint32_t c[4];
-    if (inv <= 3.0e38f) {
+    if constexpr (K == kCacheFp8) {
+      fp8_encode<16>(x, inv, inv <= 3.0e38f, c);
+    } else if (inv <= 3.0e38f) {
       // rint(fl32(x * inv)) in [-127, 127]: adding 1.5 * 2^23 rounds to an
       // integer (ties to even) whose low byte is the two's-complement code.
       // The product is rounded on its own (the packed multiply) and the add
@@ -178,7 +209,7 @@ constexpr int kAppendTokens = 2;  // tokens per block (and rows per 16-lane grou
 // consecutive ring slots.  Each lane group issues all its loads before any
 // arithmetic.
 // Many small CTAs (eight per SM for bf16 input) keep enough rows in flight.
-template <bool kF32In, bool kInt8>
+template <bool kF32In, int K>
 __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __grid_constant__ AppendParams p) {
   const int h = blockIdx.y * 16 + (threadIdx.x >> 4);
   if (h >= p.heads) return;  // whole 16-lane groups leave together
@@ -206,7 +237,7 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
-    write_row<kInt8>(p, tensor, dst_row, x[r], g, gmask);
+    write_row<K>(p, tensor, dst_row, x[r], g, gmask);
   }
 }
 
@@ -215,8 +246,8 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
 // twice as many values.  Grid: x = groups of kAppendTokens tokens, y = groups
 // of 32 heads, z = (block, tensor); a CTA's 32 row groups are consecutive
 // heads.  A BF16 cache takes the bf16 values unchanged (a copy).
-template <bool kInt8>
-__global__ void __launch_bounds__(256, kInt8 ? 6 : 8) append8_kernel(const __grid_constant__ AppendParams p) {
+template <int K>
+__global__ void __launch_bounds__(256, K != kCacheBF16 ? 6 : 8) append8_kernel(const __grid_constant__ AppendParams p) {
   const int h = blockIdx.y * 32 + (threadIdx.x >> 3);
   if (h >= p.heads) return;  // whole 8-lane groups leave together
   const int g = threadIdx.x & 7;
@@ -245,7 +276,7 @@ __global__ void __launch_bounds__(256, kInt8 ? 6 : 8) append8_kernel(const __gri
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
-    if constexpr (kInt8) {
+    if constexpr (K != kCacheBF16) {
       const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
       float x[16];
 #pragma unroll
@@ -253,7 +284,7 @@ __global__ void __launch_bounds__(256, kInt8 ? 6 : 8) append8_kernel(const __gri
         x[2 * e] = __uint_as_float(u[e] << 16);
         x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
       }
-      store_row16<true>(p, tensor, dst_row, x, g, gmask);
+      store_row16<K>(p, tensor, dst_row, x, g, gmask);
     } else {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g);
       dst[0] = w[r][0];
@@ -272,7 +303,7 @@ constexpr int kStages = 3;
 constexpr int kStagedThreads = 288;      // 8 consumer warps + 1 producer warp
 constexpr int kStageBytes = 32 * 1024;   // largest chunk
 
-template <bool kF32In, bool kInt8>
+template <bool kF32In, int K>
 __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const __grid_constant__ AppendParams p) {
   extern __shared__ __align__(128) uint8_t stage_raw[];
   __shared__ uint64_t full[kStages], empty[kStages];
@@ -362,7 +393,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const 
           if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
           const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
                                     static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
-          write_row<kInt8>(p, tensor, dst_row, x, g, gmask);
+          write_row<K>(p, tensor, dst_row, x, g, gmask);
         }
       }
       __syncwarp();
@@ -381,7 +412,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const 
 // exactly what RoPE followed by append would write.
 constexpr int kRopeAppendTokens = 8;
 
-template <bool kF32In, bool kInt8>
+template <bool kF32In, int K>
 __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant__ AppendParams p,
                                                           const __grid_constant__ RopeParams rp, TwoPi tp) {
   __shared__ float2 cs[kRopeAppendTokens][kRopeMaxPairs];  // (cos, sin) per token and pair
@@ -439,7 +470,7 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant_
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
-    write_row<kInt8>(p, tensor, dst_row, x[r], g, gmask);
+    write_row<K>(p, tensor, dst_row, x[r], g, gmask);
   }
 }
 
@@ -451,7 +482,7 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant_
 constexpr int kRope8Rows = 64;
 constexpr int kRope8MaxTokens = kRope8Rows + 1;  // tokens a 64-row range can touch (heads = 1)
 
-template <bool kInt8>
+template <int K>
 __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_constant__ AppendParams p,
                                                               const __grid_constant__ RopeParams rp, TwoPi tp) {
   __shared__ float2 cs[kRope8MaxTokens][kRopeMaxPairs];
@@ -518,7 +549,7 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
                               static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
-    store_row16<kInt8>(p, tensor, dst_row, x, g, gmask);
+    store_row16<K>(p, tensor, dst_row, x, g, gmask);
   }
 }
 
@@ -533,33 +564,74 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint8_t* __restrict__ pt
 
 }  // namespace
 
-cudaError_t launch_append_rope(bool f32_in, bool int8_cache, const AppendParams& p, const RopeParams& rp,
+cudaError_t launch_append_rope(bool f32_in, int kind, const AppendParams& p, const RopeParams& rp,
                                cudaStream_t stream) {
   if (p.n_tokens <= 0 || p.blocks <= 0 || p.heads <= 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((p.n_tokens + kRopeAppendTokens - 1) / kRopeAppendTokens),
-                  static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
-  if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+  if (kind != kCacheBF16 && kind != kCacheInt8 && kind != kCacheFp8) return cudaErrorInvalidValue;
   const TwoPi tp = rope_two_pi();
   if (f32_in) {
-    if (int8_cache)
-      append_rope_kernel<true, true><<<grid, 256, 0, stream>>>(p, rp, tp);
+    const dim3 grid(static_cast<unsigned>((p.n_tokens + kRopeAppendTokens - 1) / kRopeAppendTokens),
+                    static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
+    if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+    if (kind == kCacheInt8)
+      append_rope_kernel<true, kCacheInt8><<<grid, 256, 0, stream>>>(p, rp, tp);
+    else if (kind == kCacheFp8)
+      append_rope_kernel<true, kCacheFp8><<<grid, 256, 0, stream>>>(p, rp, tp);
     else
-      append_rope_kernel<true, false><<<grid, 256, 0, stream>>>(p, rp, tp);
+      append_rope_kernel<true, kCacheBF16><<<grid, 256, 0, stream>>>(p, rp, tp);
   } else {
     const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
     const long long cta = (rows + kRope8Rows - 1) / kRope8Rows;
-    if (cta > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (cta > 0x7FFFFFFFLL || 2LL * p.blocks > 65535) return cudaErrorInvalidValue;
     const dim3 grid8(static_cast<unsigned>(cta), 1, static_cast<unsigned>(2 * p.blocks));
-    if (int8_cache)
-      append8_rope_kernel<true><<<grid8, 256, 0, stream>>>(p, rp, tp);
+    if (kind == kCacheInt8)
+      append8_rope_kernel<kCacheInt8><<<grid8, 256, 0, stream>>>(p, rp, tp);
+    else if (kind == kCacheFp8)
+      append8_rope_kernel<kCacheFp8><<<grid8, 256, 0, stream>>>(p, rp, tp);
     else
-      append8_rope_kernel<false><<<grid8, 256, 0, stream>>>(p, rp, tp);
+      append8_rope_kernel<kCacheBF16><<<grid8, 256, 0, stream>>>(p, rp, tp);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p_in, int sms, cudaStream_t stream) {
+namespace {
+template <bool kF32In, int K>
+cudaError_t launch_staged(const AppendParams& p, unsigned grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = kStages * kStageBytes;
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(append_staged_kernel<kF32In, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  append_staged_kernel<kF32In, K><<<grid, kStagedThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t launch_direct(bool f32_in, const AppendParams& p, cudaStream_t stream) {
+  if (!f32_in) {
+    const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
+                    static_cast<unsigned>((p.heads + 31) / 32), static_cast<unsigned>(2 * p.blocks));
+    if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+    append8_kernel<K><<<grid, 256, 0, stream>>>(p);
+  } else {
+    const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
+                    static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
+    if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+    append_kernel<true, K><<<grid, 256, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_append(bool f32_in, int kind, const AppendParams& p_in, int sms, cudaStream_t stream) {
   if (p_in.n_tokens <= 0 || p_in.blocks <= 0 || p_in.heads <= 0) return cudaSuccess;
+  if (kind != kCacheBF16 && kind != kCacheInt8 && kind != kCacheFp8) return cudaErrorInvalidValue;
   AppendParams p = p_in;
   const long long token_bytes = static_cast<long long>(p.heads) * 128 * (f32_in ? 4 : 2);
   const long long in_bytes = 2LL * p.blocks * p.n_tokens * token_bytes;
@@ -570,47 +642,18 @@ cudaError_t launch_append(bool f32_in, bool int8_cache, const AppendParams& p_in
     p.chunk_tokens = static_cast<int>(kStageBytes / token_bytes);
     const long long chunks = 2LL * p.blocks * ((p.n_tokens + p.chunk_tokens - 1) / p.chunk_tokens);
     const unsigned grid = static_cast<unsigned>(chunks < 2LL * sms ? chunks : 2LL * sms);
-    static int configured[64][4] = {{0}};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const int idx = (f32_in ? 2 : 0) + (int8_cache ? 1 : 0);
-    const size_t smem = kStages * kStageBytes;
-    auto kern = f32_in ? (int8_cache ? append_staged_kernel<true, true> : append_staged_kernel<true, false>)
-                       : (int8_cache ? append_staged_kernel<false, true> : append_staged_kernel<false, false>);
-    if (dev >= 0 && dev < 64 && !configured[dev][idx]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-      configured[dev][idx] = 1;
+    if (f32_in) {
+      if (kind == kCacheInt8) return launch_staged<true, kCacheInt8>(p, grid, stream);
+      if (kind == kCacheFp8) return launch_staged<true, kCacheFp8>(p, grid, stream);
+      return launch_staged<true, kCacheBF16>(p, grid, stream);
     }
-    kern<<<grid, kStagedThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    if (kind == kCacheInt8) return launch_staged<false, kCacheInt8>(p, grid, stream);
+    if (kind == kCacheFp8) return launch_staged<false, kCacheFp8>(p, grid, stream);
+    return launch_staged<false, kCacheBF16>(p, grid, stream);
   }
-  if (!f32_in) {
-    const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
-                    static_cast<unsigned>((p.heads + 31) / 32), static_cast<unsigned>(2 * p.blocks));
-    if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
-    if (int8_cache)
-      append8_kernel<true><<<grid, 256, 0, stream>>>(p);
-    else
-      append8_kernel<false><<<grid, 256, 0, stream>>>(p);
-    return cudaGetLastError();
-  }
-  const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
-                  static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
-  if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
-  if (f32_in) {
-    if (int8_cache)
-      append_kernel<true, true><<<grid, 256, 0, stream>>>(p);
-    else
-      append_kernel<true, false><<<grid, 256, 0, stream>>>(p);
-  } else {
-    if (int8_cache)
-      append_kernel<false, true><<<grid, 256, 0, stream>>>(p);
-    else
-      append_kernel<false, false><<<grid, 256, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (kind == kCacheInt8) return launch_direct<kCacheInt8>(f32_in, p, stream);
+  if (kind == kCacheFp8) return launch_direct<kCacheFp8>(f32_in, p, stream);
+  return launch_direct<kCacheBF16>(f32_in, p, stream);
 }
 
 cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream) {

@@ -71,6 +71,13 @@ nomas_status encoder(EncodeTiledFn* fn) {
   return NOMAS_OK;
 }
 
+// One-byte codes with per-row scales (INT8 or FP8) rather than bf16 values.
+bool quantised(const nomas_kvcache* c) { return c->dtype == NOMAS_INT8 || c->dtype == NOMAS_FP8; }
+
+int cache_kind(const nomas_kvcache* c) {
+  return c->dtype == NOMAS_INT8 ? kCacheInt8 : (c->dtype == NOMAS_FP8 ? kCacheFp8 : kCacheBF16);
+}
+
 int64_t window_of(const nomas_kvcache* c) { return c->past_frames > 0 ? c->past_frames : c->capacity_frames; }
 
 nomas_status validate_cache(const nomas_kvcache* c) {
@@ -81,13 +88,13 @@ nomas_status validate_cache(const nomas_kvcache* c) {
   if (c->head_dim <= 0) return NOMAS_ERR_INVALID_ARG;
   if (c->head_dim != 128) return NOMAS_ERR_UNSUPPORTED;
   if (c->past_frames > 0 && c->capacity_frames != c->past_frames) return NOMAS_ERR_INVALID_ARG;
-  if (c->dtype != NOMAS_INT8 && c->dtype != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
+  if (c->dtype != NOMAS_INT8 && c->dtype != NOMAS_BF16 && c->dtype != NOMAS_FP8) return NOMAS_ERR_INVALID_ARG;
   const int64_t tpf = static_cast<int64_t>(c->grid_h) * c->grid_w;
   const int64_t slots = tpf * c->capacity_frames;
   if (slots > (int64_t(1) << 30) || static_cast<int64_t>(c->num_blocks) * c->heads > (int64_t(1) << 24))
     return NOMAS_ERR_UNSUPPORTED;
   if (c->k == nullptr || c->v == nullptr || !aligned16(c->k) || !aligned16(c->v)) return NOMAS_ERR_INVALID_ARG;
-  if (c->dtype == NOMAS_INT8) {
+  if (quantised(c)) {
     if (c->k_scale == nullptr || c->v_scale == nullptr) return NOMAS_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(c->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(c->v_scale) & 3u))
       return NOMAS_ERR_INVALID_ARG;
@@ -197,7 +204,7 @@ NOMAS_API size_t nomas_kvcache_bytes(const nomas_kvcache* c) {
       c->capacity_frames <= 0)
     return 0;
   const size_t rows = static_cast<size_t>(c->num_blocks) * c->heads * c->grid_h * c->grid_w * c->capacity_frames;
-  if (c->dtype == NOMAS_INT8) return 2 * rows * (static_cast<size_t>(c->head_dim) + 4);
+  if (quantised(c)) return 2 * rows * (static_cast<size_t>(c->head_dim) + 4);
   if (c->dtype == NOMAS_BF16) return 2 * rows * static_cast<size_t>(c->head_dim) * 2;
   return 0;
 }
@@ -316,9 +323,9 @@ nomas_status append_impl(nomas_kvcache* cache, const void* k, const void* v, nom
       rp.heads = cache->heads;
       rp.n_video = p.n_tokens;
       rp.row_stride = static_cast<long long>(cache->heads) * cache->head_dim;
-      st = from_cuda(launch_append_rope(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, rp, stream));
+      st = from_cuda(launch_append_rope(in_dt == NOMAS_F32, cache_kind(cache), p, rp, stream));
     } else {
-      st = from_cuda(launch_append(in_dt == NOMAS_F32, cache->dtype == NOMAS_INT8, p, sms, stream));
+      st = from_cuda(launch_append(in_dt == NOMAS_F32, cache_kind(cache), p, sms, stream));
     }
     if (st != NOMAS_OK) return st;
   }
@@ -349,7 +356,7 @@ NOMAS_API nomas_status nomas_kvcache_append_rope(nomas_kvcache* cache, const voi
 }
 
 NOMAS_API size_t nomas_kvcache_archive_frame_bytes(const nomas_kvcache* c) {
-  if (validate_cache(c) != NOMAS_OK || c->dtype != NOMAS_INT8) return 0;
+  if (validate_cache(c) != NOMAS_OK || !quantised(c)) return 0;
   const size_t rows = static_cast<size_t>(c->num_blocks) * c->heads * c->grid_h * c->grid_w;
   return 2 * rows * (static_cast<size_t>(c->head_dim) + 4);
 }
@@ -360,7 +367,7 @@ NOMAS_API nomas_status nomas_kvcache_append_archive(nomas_kvcache* cache, const 
                                                     cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
-  if (cache->dtype != NOMAS_INT8) return NOMAS_ERR_UNSUPPORTED;
+  if (!quantised(cache)) return NOMAS_ERR_UNSUPPORTED;
   if (archive == nullptr || archive_used == nullptr || n_frames < 0) return NOMAS_ERR_INVALID_ARG;
   if (in_dt != NOMAS_F32 && in_dt != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
   st = plan(cache, n_frames, nullptr, nullptr, nullptr, nullptr);
@@ -417,10 +424,10 @@ NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory
   if (zero_memory) {
     const size_t rows = static_cast<size_t>(cache->num_blocks) * cache->heads * cache->grid_h * cache->grid_w *
                         cache->capacity_frames;
-    const size_t kv_bytes = rows * cache->head_dim * (cache->dtype == NOMAS_INT8 ? 1 : 2);
+    const size_t kv_bytes = rows * cache->head_dim * (quantised(cache) ? 1 : 2);
     st = from_cuda(launch_zero_fill(cache->k, kv_bytes, stream));
     if (st == NOMAS_OK) st = from_cuda(launch_zero_fill(cache->v, kv_bytes, stream));
-    if (st == NOMAS_OK && cache->dtype == NOMAS_INT8) {
+    if (st == NOMAS_OK && quantised(cache)) {
       st = from_cuda(launch_zero_fill(cache->k_scale, rows * 4, stream));
       if (st == NOMAS_OK) st = from_cuda(launch_zero_fill(cache->v_scale, rows * 4, stream));
     }
@@ -484,7 +491,7 @@ nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const 
     if (num_splits > 1) return NOMAS_ERR_INVALID_ARG;  // an explicit split count needs its workspace
     pl = attn_plan(cache, n_video, n_text, 1, sms);
   }
-  const bool int8 = cache->dtype == NOMAS_INT8;
+  const bool int8 = quantised(cache);  // one-byte codes (INT8 or FP8): staged and dequantised in the kernel
   AttnTensorMaps tm;
   memset(&tm, 0, sizeof(tm));
   const uint64_t H = cache->heads;
@@ -537,7 +544,7 @@ nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const 
   p.sparse_counts = counts;
   p.max_keep = max_keep;
   p.n_groups = (pl.nq + 511) / 512;
-  st = from_cuda(launch_segment_attn(int8, tm, p, pl.n_pairs, stream));
+  st = from_cuda(launch_segment_attn(cache_kind(cache), tm, p, pl.n_pairs, stream));
   if (st == NOMAS_OK && pl.splits > 1) st = from_cuda(launch_attn_combine(p, stream));
   return st;
 }
@@ -609,7 +616,7 @@ NOMAS_API nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t b
     // Nothing resident: every list is empty.
     return from_cuda(cudaMemsetAsync(counts, 0, static_cast<size_t>(cache->heads) * n_groups * 4, stream));
   }
-  return from_cuda(launch_sparse_select(cache->dtype == NOMAS_INT8, reuse_key_means != 0, p, stream));
+  return from_cuda(launch_sparse_select(cache_kind(cache), reuse_key_means != 0, p, stream));
 }
 
 NOMAS_API nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int32_t block, const void* q,

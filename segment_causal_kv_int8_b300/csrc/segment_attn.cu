@@ -29,6 +29,8 @@
 // memory and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -134,7 +136,7 @@ __device__ __forceinline__ float i8_to_f32(uint32_t biased, uint32_t sel) {
   return __uint_as_float(__byte_perm(biased, 0x4B000000u, sel)) - 8388736.0f;
 }
 
-template <bool kInt8>
+template <bool kInt8, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     segment_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcur,
                         const __grid_constant__ CUtensorMap tm_vcur, const __grid_constant__ CUtensorMap tm_kc,
@@ -594,16 +596,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = 0; cc < 4; ++cc) {
             const int c = 4 * half + cc;  // int8 chunk: columns 16c .. 16c+15
             const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw_src) << 4));
-            const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
             uint32_t o[8];
+            if constexpr (kFp8) {
+              // E4M3 pairs -> f16 pairs (exact) -> float32, times the row scale.
+              const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float f0 = i8_to_f32(wd[e], 0x7540u) * sc;
-              const float f1 = i8_to_f32(wd[e], 0x7541u) * sc;
-              const float f2 = i8_to_f32(wd[e], 0x7542u) * sc;
-              const float f3 = i8_to_f32(wd[e], 0x7543u) * sc;
-              o[2 * e] = pack_bf16x2(f0, f1);
-              o[2 * e + 1] = pack_bf16x2(f2, f3);
+              for (int e = 0; e < 4; ++e) {
+                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>(wd[e] & 0xFFFFu), __NV_E4M3);
+                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wd[e] >> 16),
+                                                                  __NV_E4M3);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+                o[2 * e] = pack_bf16x2(a.x * sc, a.y * sc);
+                o[2 * e + 1] = pack_bf16x2(b.x * sc, b.y * sc);
+              }
+            } else {
+              const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float f0 = i8_to_f32(wd[e], 0x7540u) * sc;
+                const float f1 = i8_to_f32(wd[e], 0x7541u) * sc;
+                const float f2 = i8_to_f32(wd[e], 0x7542u) * sc;
+                const float f3 = i8_to_f32(wd[e], 0x7543u) * sc;
+                o[2 * e] = pack_bf16x2(f0, f1);
+                o[2 * e + 1] = pack_bf16x2(f2, f3);
+              }
             }
             // 16 int8 columns -> 16-byte chunks 2cc and 2cc+1 of bf16 panel `half`
             *reinterpret_cast<uint4*>(dst + ((((2 * cc) ^ sw_dst)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -700,7 +718,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (lse && lane == 0) lse[static_cast<size_t>(h) * nq + r] = mx + logf(wsum);
 }
 
-template <bool kInt8>
+template <bool kInt8, bool kFp8>
 static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, int n_pairs, cudaStream_t stream) {
   using L = Layout<kInt8>;
   static int configured[64] = {0};
@@ -709,7 +727,8 @@ static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, in
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(segment_attn_kernel<kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    e = cudaFuncSetAttribute(segment_attn_kernel<kInt8, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -728,21 +747,24 @@ static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, segment_attn_kernel<kInt8>, tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
+    e = cudaLaunchKernelEx(&cfg, segment_attn_kernel<kInt8, kFp8>, tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
     if (e != cudaSuccess) return e;
   } else {
     dim3 grid(n_pairs, p.heads, p.num_splits);
-    segment_attn_kernel<kInt8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
+    segment_attn_kernel<kInt8, kFp8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc,
+                                                                             p);
   }
   return cudaGetLastError();
 }
 
 }  // namespace attn
 
-cudaError_t launch_segment_attn(bool int8_cache, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
+cudaError_t launch_segment_attn(int kind, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
                                 cudaStream_t stream) {
-  return int8_cache ? attn::launch_impl<true>(tm, p, n_pairs, stream)
-                    : attn::launch_impl<false>(tm, p, n_pairs, stream);
+  if (kind == kCacheInt8) return attn::launch_impl<true, false>(tm, p, n_pairs, stream);
+  if (kind == kCacheFp8) return attn::launch_impl<true, true>(tm, p, n_pairs, stream);
+  if (kind == kCacheBF16) return attn::launch_impl<false, false>(tm, p, n_pairs, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream) {

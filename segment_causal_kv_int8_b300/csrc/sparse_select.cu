@@ -11,7 +11,8 @@
 // tile order.
 //
 // Two HBM-bound kernels.  tile_means_kernel reads the resident cache K once
-// (16-byte coalesced loads, int8 codes dequantised with their row scale) and
+// (16-byte coalesced loads, INT8 or FP8 codes dequantised with their row
+// scale) and
 // writes the float32 mean key of every (head, tile); the means depend only on
 // the cache, so callers may keep them across the denoising steps of a turn.
 // select_kernel, one CTA per (query group, head), reads the group's queries
@@ -19,6 +20,8 @@
 // every tile, ranks the scores and writes the kept list with a block-wide
 // prefix count.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -43,9 +46,10 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& w) {
 // lanes cover a 128-byte row, 32 rows at a time (4 passes); each code is
 // multiplied by its row scale before it is summed.  Partial sums (one per
 // row lane) are added in a fixed order in shared memory.
-template <bool kInt8>
+template <int K>
 __global__ void __launch_bounds__(kSelThreads) tile_means_kernel(const SparseSelectParams p) {
-  constexpr int kLanesPerRow = kInt8 ? 8 : 16;    // 16-byte vectors per row
+  constexpr bool kCodes = K != kCacheBF16;        // one-byte codes (INT8 or FP8) with row scales
+  constexpr int kLanesPerRow = kCodes ? 8 : 16;   // 16-byte vectors per row
   constexpr int kDims = 128 / kLanesPerRow;       // dims per thread
   constexpr int kRowSlots = kSelThreads / kLanesPerRow;
   __shared__ float part[kRowSlots][129];
@@ -61,7 +65,7 @@ __global__ void __launch_bounds__(kSelThreads) tile_means_kernel(const SparseSel
     const int r = pass * kRowSlots + rs;
     if (r < n) {
       const long long row = plane + r0 + r;
-      if constexpr (kInt8) {
+      if constexpr (K == kCacheInt8) {
         const uint4 w = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(p.kcache) + row * 128)[c];
         const float s = p.kscale[row];
         const uint32_t v[4] = {w.x, w.y, w.z, w.w};
@@ -69,6 +73,18 @@ __global__ void __launch_bounds__(kSelThreads) tile_means_kernel(const SparseSel
         for (int e = 0; e < 16; ++e) {
           const int8_t code = static_cast<int8_t>((v[e >> 2] >> (8 * (e & 3))) & 0xFFu);
           acc[e] += static_cast<float>(code) * s;
+        }
+      } else if constexpr (K == kCacheFp8) {
+        const uint4 w = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.kcache) + row * 128)[c];
+        const float s = p.kscale[row];
+        const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(
+              static_cast<__nv_fp8x2_storage_t>((v[e >> 1] >> (16 * (e & 1))) & 0xFFFFu), __NV_E4M3);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          acc[2 * e] += f.x * s;
+          acc[2 * e + 1] += f.y * s;
         }
       } else {
         const uint4 w = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.kcache) + row * 128)[c];
@@ -220,14 +236,16 @@ size_t sparse_select_smem(int n_tiles) {
   return ((need > part ? need : part) + 15) & ~size_t(15);
 }
 
-cudaError_t launch_sparse_select(bool int8_cache, bool reuse_key_means, const SparseSelectParams& p,
+cudaError_t launch_sparse_select(int kind, bool reuse_key_means, const SparseSelectParams& p,
                                  cudaStream_t stream) {
   if (p.n_tiles > 0 && !reuse_key_means) {
     const dim3 tg(p.n_tiles, p.heads);
-    if (int8_cache)
-      tile_means_kernel<true><<<tg, kSelThreads, 0, stream>>>(p);
+    if (kind == kCacheInt8)
+      tile_means_kernel<kCacheInt8><<<tg, kSelThreads, 0, stream>>>(p);
+    else if (kind == kCacheFp8)
+      tile_means_kernel<kCacheFp8><<<tg, kSelThreads, 0, stream>>>(p);
     else
-      tile_means_kernel<false><<<tg, kSelThreads, 0, stream>>>(p);
+      tile_means_kernel<kCacheBF16><<<tg, kSelThreads, 0, stream>>>(p);
   }
   const dim3 gg(p.n_groups, p.heads);
   select_kernel<<<gg, kPickThreads, sparse_select_smem(p.n_tiles), stream>>>(p);

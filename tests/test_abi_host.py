@@ -184,3 +184,17 @@ def test_sparse_entry_points_validate_before_launching():
                                            None, None, 0, 0, None) == nomas.NOMAS_ERR_INVALID_ARG
     assert nomas.nomas_segment_attn_sparse(ctypes.byref(d), 0, 256, 256, 256, 7360, 256, 0.1, 256, 256, 0, 256,
                                            None, None, 0, 0, None) == nomas.NOMAS_ERR_INVALID_ARG
+
+
+def test_fp8_descriptor_is_a_quantised_cache():
+    d = _desc(dtype=nomas.NOMAS_FP8)
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_OK
+    i8 = _desc(dtype=nomas.NOMAS_INT8)
+    assert nomas.nomas_kvcache_bytes(ctypes.byref(d)) == nomas.nomas_kvcache_bytes(ctypes.byref(i8))
+    assert nomas.nomas_kvcache_archive_frame_bytes(ctypes.byref(d)) == 2 * 1 * 2 * 12 * (128 + 4)
+    d.k_scale = None  # scales are required, as for INT8
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_ERR_INVALID_ARG
+    # an FP8 input dtype is not an input format
+    d = _desc(dtype=nomas.NOMAS_FP8)
+    assert nomas.nomas_kvcache_append(ctypes.byref(d), 256, 256, nomas.NOMAS_FP8, 1, 0,
+                                      None) == nomas.NOMAS_ERR_INVALID_ARG

@@ -67,7 +67,7 @@ def test_rope3d_large_frame_index_and_odd_split():
 
 # ------------------------------------------------------------------ append
 def _check_cache_bits(gc, oc):
-    if oc.dtype == "int8":
+    if oc.dtype in ("int8", "fp8"):
         np.testing.assert_array_equal(gc.k.cpu().numpy(), oc.k_codes)
         np.testing.assert_array_equal(gc.v.cpu().numpy(), oc.v_codes)
         np.testing.assert_array_equal(gc.k_scale.cpu().numpy().view(np.uint32), oc.k_scales.view(np.uint32))
@@ -86,7 +86,7 @@ def test_append_bit_exact(name):
 
 
 @pytest.mark.parametrize("in_dtype,cache_dtype", [("f32", "int8"), ("bf16", "int8"), ("f32", "bf16"),
-                                                  ("bf16", "bf16")])
+                                                  ("bf16", "bf16"), ("f32", "fp8"), ("bf16", "fp8")])
 def test_append_multi_block_window_wrap_and_long_segment(in_dtype, cache_dtype):
     # 3 blocks, window 4 frames: segments of 3, 2, 6 (longer than the window), 1 frames.
     blocks, heads, gh, gw, W = 3, 2, 3, 5, 4
@@ -106,9 +106,10 @@ def test_append_multi_block_window_wrap_and_long_segment(in_dtype, cache_dtype):
         _check_cache_bits(gc, oc)
 
 
-def test_append_codec_edge_rows():
-    heads, gh, gw = 1, 1, 8
-    rows = np.zeros((8, 128), np.float32)
+@pytest.mark.parametrize("cache_dtype", ["int8", "fp8"])
+def test_append_codec_edge_rows(cache_dtype):
+    heads, gh, gw = 1, 1, 9
+    rows = np.zeros((9, 128), np.float32)
     rows[1, :8] = [127.0, 2.5, 3.5, -2.5, -0.5, 0.5, 126.5, -1.5]          # ties (inv = 1)
     rows[2] = np.linspace(-1e-39, 1e-39, 128, dtype=np.float32)              # subnormal, inv overflows
     rows[3] = np.linspace(-3e-37, 2e-37, 128, dtype=np.float32)              # tiny normal
@@ -116,9 +117,12 @@ def test_append_codec_edge_rows():
     rows[5, 17] = -8.0                                                       # single negative spike
     rows[6] = np.arange(-64, 64, dtype=np.float32)
     rows[7] = -rows[6]
-    k = rows.reshape(1, 8, 1, 128)
-    gc = nomas.KVCache(1, heads, gh, gw, 1, 0, "int8")
-    oc = ring_cache.RingCache(1, heads, 128, gh, gw, 1, 0, "int8")
+    # absmax 448 (inv = 1 for FP8): E4M3 midpoints, subnormal midpoints, signed zero
+    rows[8, :10] = [448.0, 1.0625, -1.0625, 7.5 * 2.0 ** -9, 0.5 * 2.0 ** -9, -0.5 * 2.0 ** -9, 1.5 * 2.0 ** -9,
+                    232.0, -0.0, 3.0 * 2.0 ** -10]
+    k = rows.reshape(1, 9, 1, 128)
+    gc = nomas.KVCache(1, heads, gh, gw, 1, 0, cache_dtype)
+    oc = ring_cache.RingCache(1, heads, 128, gh, gw, 1, 0, cache_dtype)
     gc.append(to_dev(k, "f32"), to_dev(k, "f32"))
     oc.append(k, k)
     _check_cache_bits(gc, oc)
