@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
     ap.add_argument("--cache-dtype", choices=["int8", "fp8", "bf16"], default=None,
                     help="override the config's cache format (fp8: the E4M3 comparison variant)")
+    ap.add_argument("--camera", type=int, default=0,
+                    help="add the camera cross-attention with this many camera tokens per latent frame to the step")
     ap.add_argument("--append-rope", action="store_true",
                     help="write the history with the fused RoPE + append (keys rotated on the way into the cache)")
     ap.add_argument("--sparse", type=float, default=0.0,
@@ -271,6 +273,13 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
+    if args.camera:
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed)
+        cam_k = torch.randn((wl.cur_frames, args.camera, wl.heads, wl.head_dim), generator=g, device=dev).to(
+            torch.bfloat16)
+        cam_v = torch.randn(cam_k.shape, generator=g, device=dev).to(torch.bfloat16)
+        cam_out = torch.empty((wl.n_video, wl.heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
     keep = args.sparse
     if keep:
         import ctypes
@@ -326,6 +335,12 @@ def run_ours(args):
                                num_splits=args.num_splits)
         if ev is not None:
             ev[5].record(stream)
+        if args.camera:
+            if ev is not None:
+                ev[8].record(stream)
+            nomas.camera_cross_attn(q, cam_k, cam_v, wl.cur_frames, wl.grid_h, wl.grid_w, out=cam_out)
+            if ev is not None:
+                ev[9].record(stream)
 
     def restage():
         q.copy_(q0)  # RoPE works in place: fresh un-rotated inputs for every step (untimed)
@@ -337,7 +352,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(dev.index if world == 1 else local)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -361,6 +376,7 @@ def run_ours(args):
     rope_ms = [e[4].elapsed_time(e[5]) for e in evs]
     attn_ms = [e[6].elapsed_time(e[7]) for e in evs]
     select_ms = [e[8].elapsed_time(e[9]) for e in evs] if keep else None
+    camera_ms = [e[10].elapsed_time(e[11]) for e in evs] if args.camera else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -378,7 +394,8 @@ def run_ours(args):
     if not args.no_e2e and not keep and not args.append_rope:
         e2e = _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world)
 
-    launches_per_step = len(hist) + 1 + 1 + (1 if splits_used > 1 else 0) + (3 if keep and wl.n_cache else 0)
+    launches_per_step = (len(hist) + 1 + 1 + (1 if splits_used > 1 else 0) + (2 if keep and wl.n_cache else 0)
+                         + (1 if args.camera else 0))
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -395,6 +412,14 @@ def run_ours(args):
                              "peak": hbm, "unit": "GB/s", "frac": gbs / hbm if gbs else None,
                              "launches_per_step": len(hist) if name == append_name else 1}
     # the committed counters describe the config's own cache format
+    if args.camera:
+        t = statistics.mean(camera_ms)
+        nbytes = 2 * wl.n_video * wl.heads * wl.head_dim * 2 + 2 * wl.cur_frames * args.camera * wl.heads * wl.head_dim * 2
+        gbs = nbytes / (t * 1e-3) / 1e9 if t > 0 else None
+        elementwise["camera_cross_attn"] = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": 1e3 * t,
+                                            "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                            "frac": gbs / hbm if gbs else None, "launches_per_step": 1,
+                                            "camera_tokens_per_frame": args.camera}
     traffic = _load_traffic(args.config) if wl.cache_dtype == CONFIGS[args.config].cache_dtype else None
     if rank == 0:
         line = {

@@ -345,6 +345,30 @@ nomas_status nomas_segment_attn_noalloc(const nomas_kvcache* cache, int32_t bloc
                                         int32_t num_splits, cudaStream_t stream);
 
 /*
+ * Camera cross-attention of the current segment's video tokens.  Camera
+ * control enters as 4x4 extrinsic matrices grouped over four frames and fed
+ * through cross-attention in every block (blog.authon.dev guide, section
+ * "What Hy-Nomas is", model-card specs); one latent frame covers four video
+ * frames (4x temporal compression, same list).  Reading: the camera encoder
+ * (trained weights, upstream of this call) gives each latent frame n_cam
+ * key/value tokens per head, and every video token of latent frame f attends
+ * to exactly those: per head, O = softmax(s q K_f^T) V_f.  Text tokens are
+ * not involved.
+ *
+ *   q            device bf16 [frames * grid_h * grid_w][heads][128]: the
+ *                video rows (the first rows of a segment's Q tensor)
+ *   k_cam, v_cam device bf16 [frames][n_cam][heads][128]
+ *   n_cam        camera tokens per latent frame, 1 .. 16
+ *   softmax_scale s > 0
+ *   out          device bf16 [frames * grid_h * grid_w][heads][128]
+ * float32 arithmetic, bf16 output.  NOMAS_ERR_UNSUPPORTED for n_cam > 16.
+ */
+nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam, const void* v_cam,
+                                     int32_t frames, int32_t grid_h, int32_t grid_w,
+                                     int32_t heads, int32_t n_cam, float softmax_scale,
+                                     void* out, cudaStream_t stream);
+
+/*
  * Start a new session (the resident service's new session_id, "Setup" and the
  * JSON turns on the inferencekey.com RTX 4090 test page): total_frames and
  * valid_frames to 0; with zero_memory != 0 also enqueue a kernel that clears

@@ -93,6 +93,7 @@ EXPORTS = {
                                      _sz, _vp]),
     "nomas_segment_attn_sparse": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
                                            _i32, _vp, _vp, _vp, _sz, _i32, _vp]),
+    "nomas_camera_cross_attn": (_c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
     "nomas_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _vp]),
     "nomas_device_error": (_c_int, [_P(_c_int), _c_int]),
@@ -382,6 +383,36 @@ def segment_attn_sparse(cache: KVCache, block: int, q, k_cur, v_cur, n_video: in
     return out
 
 
+def camera_cross_attn(q, k_cam, v_cam, frames: int, grid_h: int, grid_w: int, softmax_scale: Optional[float] = None,
+                      out=None, stream=None):
+    """Cross-attention of the video rows of ``q`` to their latent frame's camera tokens.
+
+    ``q``: bf16 ``[>= frames*grid_h*grid_w][heads][128]`` (video rows first);
+    ``k_cam``/``v_cam``: bf16 ``[frames][n_cam][heads][128]``.  Returns ``out``,
+    bf16 ``[frames*grid_h*grid_w][heads][128]``.
+    """
+    torch = _torch()
+    for t in (q, k_cam, v_cam):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k_cam, v_cam must be contiguous bfloat16 CUDA tensors")
+    nv = frames * grid_h * grid_w
+    heads = q.shape[1]
+    if q.dim() != 3 or q.shape[0] < nv or q.shape[2] != 128:
+        raise ValueError("q must be [tokens][heads][128] with at least frames*grid_h*grid_w rows")
+    if k_cam.dim() != 4 or tuple(k_cam.shape[::2]) != (frames, heads) or k_cam.shape[3] != 128 \
+            or k_cam.shape != v_cam.shape:
+        raise ValueError("k_cam/v_cam must be [frames][n_cam][heads][128]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(128)
+    if out is None:
+        out = torch.empty((nv, heads, 128), dtype=torch.bfloat16, device=q.device)
+    _check(nomas_camera_cross_attn(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_cam.data_ptr()),
+                                   ctypes.c_void_p(v_cam.data_ptr()), frames, grid_h, grid_w, heads, k_cam.shape[1],
+                                   softmax_scale, ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)),
+           "nomas_camera_cross_attn")
+    return out
+
+
 def device_error(clear: bool = True) -> int:
     """The device-side error word (0 = none), read synchronously."""
     st = ctypes.c_int(0)
@@ -390,5 +421,6 @@ def device_error(clear: bool = True) -> int:
 
 
 __all__ = ["KVCache", "rope3d", "segment_attn", "sparse_select", "segment_attn_sparse", "sparse_keep_count",
+           "camera_cross_attn",
            "device_error", "NomasError", "nomas_kvcache", "EXPORTS",
            "LIB_PATH"] + list(EXPORTS)

@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libnomas.so")
-SOURCES = ["nomas_abi.cu", "rope3d.cu", "kvcache_append.cu", "segment_attn.cu", "sparse_select.cu", "selftest.cu"]
+SOURCES = ["nomas_abi.cu", "rope3d.cu", "kvcache_append.cu", "segment_attn.cu", "sparse_select.cu", "camera_attn.cu", "selftest.cu"]
 HEADERS = ["kernels.h", "sm100.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -87,6 +87,21 @@ size_t sparse_select_smem(int n_tiles);
 cudaError_t launch_sparse_select(int kind, bool reuse_key_means, const SparseSelectParams& p,
                                  cudaStream_t stream);
 
+// ------------------------------------------------------------------ camera cross-attention
+struct CameraAttnParams {
+  const void* q;                 // bf16 [frames * tpf][heads][128] (video rows)
+  const void* k_cam;             // bf16 [frames][n_cam][heads][128]
+  const void* v_cam;
+  void* out;                     // bf16 [frames * tpf][heads][128]
+  int frames;
+  int tpf;
+  int heads;
+  int n_cam;                     // camera tokens per latent frame, 1 .. 16
+  float scale_log2;              // softmax scale * log2(e)
+};
+
+cudaError_t launch_camera_attn(const CameraAttnParams& p, cudaStream_t stream);
+
 // ------------------------------------------------------------------ attention
 struct AttnTensorMaps {
   CUtensorMap q, kcur, vcur, kc, vc;

@@ -418,6 +418,29 @@ NOMAS_API nomas_status nomas_kvcache_append_archive(nomas_kvcache* cache, const 
   return NOMAS_OK;
 }
 
+NOMAS_API nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam, const void* v_cam, int32_t frames,
+                                               int32_t grid_h, int32_t grid_w, int32_t heads, int32_t n_cam,
+                                               float softmax_scale, void* out, cudaStream_t stream) {
+  if (frames < 0 || grid_h <= 0 || grid_w <= 0 || heads <= 0 || n_cam <= 0) return NOMAS_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || !isfinite(softmax_scale)) return NOMAS_ERR_INVALID_ARG;
+  if (n_cam > 16 || heads > 65535 * 4 || frames > 65535) return NOMAS_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(grid_h) * grid_w > (int64_t(1) << 30)) return NOMAS_ERR_UNSUPPORTED;
+  if (frames == 0) return NOMAS_OK;
+  if (q == nullptr || k_cam == nullptr || v_cam == nullptr || out == nullptr) return NOMAS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cam) || !aligned16(v_cam) || !aligned16(out)) return NOMAS_ERR_INVALID_ARG;
+  CameraAttnParams p;
+  p.q = q;
+  p.k_cam = k_cam;
+  p.v_cam = v_cam;
+  p.out = out;
+  p.frames = frames;
+  p.tpf = grid_h * grid_w;
+  p.heads = heads;
+  p.n_cam = n_cam;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  return from_cuda(launch_camera_attn(p, stream));
+}
+
 NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
