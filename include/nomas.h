@@ -109,7 +109,7 @@ const char* nomas_status_string(nomas_status s);
 nomas_status nomas_kvcache_validate(const nomas_kvcache* cache);
 
 /* Device bytes the descriptor's k, v (and scales) need; 0 if invalid. Host only.
- * INT8: 2 * blocks*heads*slots*(head_dim + 4); BF16: 2 * blocks*heads*slots*head_dim*2,
+ * INT8 / FP8: 2 * blocks*heads*slots*(head_dim + 4); BF16: 2 * blocks*heads*slots*head_dim*2,
  * slots = capacity_frames*grid_h*grid_w. */
 size_t nomas_kvcache_bytes(const nomas_kvcache* cache);
 
@@ -153,7 +153,8 @@ nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, int32_t n_v
 /*
  * Append a finished segment's K/V for all blocks (the KV-cache write stage,
  * "Zeiten" on the inferencekey.com RTX 4090 test page), quantising to INT8
- * with per-(block, head, token) scales or copying to BF16, into the ring; frames
+ * (or FP8) with per-(block, head, token) scales or copying to BF16, into the
+ * ring; frames
  * older than the window are never written (a segment longer than the window
  * writes only its last past_frames frames).  Updates cache->total_frames and
  * cache->valid_frames after a successful enqueue.
@@ -196,13 +197,13 @@ nomas_status nomas_kvcache_append_rope(nomas_kvcache* cache, const void* k, cons
  *
  * nomas_kvcache_archive_frame_bytes: host bytes one archived frame takes,
  * 2 * blocks * heads * grid_h * grid_w * (head_dim + 4); 0 for an invalid or
- * non-INT8 descriptor.  Host only.
+ * BF16 descriptor.  Host only.
  *
- * nomas_kvcache_append_archive: nomas_kvcache_append of an INT8 cache that
+ * nomas_kvcache_append_archive: nomas_kvcache_append of an INT8 (or FP8) cache that
  * also copies every frame of the segment, once quantised, to host memory at
  * archive + *archive_used, in increasing frame order, and advances
  * *archive_used.  One archived frame is: K codes, V codes
- * ([blocks][heads][grid_h*grid_w][head_dim] int8 each), then K scales, V
+ * ([blocks][heads][grid_h*grid_w][head_dim] bytes each), then K scales, V
  * scales ([blocks][heads][grid_h*grid_w] float32 each).  The segment is
  * appended in chunks of at most one window, so frames that fall out of the
  * window within the segment are still archived; the cache ends in the same
@@ -232,7 +233,7 @@ nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int3
  * Segment attention of one block (the "segment-wise causal joint attention"
  * of the madebyagents.com model page over the lifelong cache of the
  * orcarouter.ai explainer): per head, O = softmax(s * Q K^T) V over the keys
- * [resident cache of `block` (dequantised if INT8) ; current segment's K/V],
+ * [resident cache of `block` (dequantised if INT8 or FP8) ; current segment's K/V],
  * every current query seeing every key of that set.
  *
  *   q, k_cur, v_cur  device bf16 [n_video + n_text][heads][head_dim]
@@ -262,7 +263,7 @@ nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const
  * [128 t, 128 t + 128) of the resident cache, the last one partial); the
  * current segment's own keys are always attended.  Queries form groups of 512
  * rows (g = row / 512).  For head h and group g, tile t scores
- * mean_query(h, g) . mean_key(h, t) (INT8 keys dequantised), and the
+ * mean_query(h, g) . mean_key(h, t) (INT8 / FP8 keys dequantised), and the
  * k = min(T, ceil(keep_fraction * T)) best tiles are kept (equal scores: the
  * lower tile first), listed in increasing tile order.
  *

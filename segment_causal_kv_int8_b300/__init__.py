@@ -243,7 +243,7 @@ class KVCache:
         return int(nomas_kvcache_archive_frame_bytes(ctypes.byref(self.desc)))
 
     def append_archive(self, k, v, archive, used: int = 0, stream=None) -> int:
-        """Append like :meth:`append` (INT8 cache) and copy every frame of the segment to ``archive``
+        """Append like :meth:`append` (INT8 or FP8 cache) and copy every frame of the segment to ``archive``
         (a host uint8 tensor, pinned for asynchronous copies) from byte ``used`` on; returns the new
         byte count.  Synchronise the stream before reading the archive."""
         if k.dim() == 3:
