@@ -198,3 +198,18 @@ def test_fp8_descriptor_is_a_quantised_cache():
     d = _desc(dtype=nomas.NOMAS_FP8)
     assert nomas.nomas_kvcache_append(ctypes.byref(d), 256, 256, nomas.NOMAS_FP8, 1, 0,
                                       None) == nomas.NOMAS_ERR_INVALID_ARG
+
+
+def test_descriptor_round_trips_through_its_bytes():
+    # the session state's host half is a plain struct: its bytes restore it
+    d = _desc(heads=16, gh=23, gw=40, cap=18, past=18, total=40, valid=18)
+    r = nomas.nomas_kvcache.from_buffer_copy(bytes(d))
+    assert nomas.nomas_kvcache_validate(ctypes.byref(r)) == nomas.NOMAS_OK
+    outs = []
+    for desc in (d, r):
+        ff, sf, vt = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        nt = ctypes.c_int64()
+        assert nomas.nomas_kvcache_plan_append(ctypes.byref(desc), 8, ctypes.byref(ff), ctypes.byref(sf),
+                                               ctypes.byref(nt), ctypes.byref(vt)) == nomas.NOMAS_OK
+        outs.append((ff.value, sf.value, nt.value, vt.value))
+    assert outs[0] == outs[1] == (0, 40 % 18, 48, 18)
