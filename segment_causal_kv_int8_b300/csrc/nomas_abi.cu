@@ -591,10 +591,9 @@ NOMAS_API nomas_status nomas_sparse_select_workspace_bytes(const nomas_kvcache* 
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
   if (bytes == nullptr || n_video < 0 || n_text < 0) return NOMAS_ERR_INVALID_ARG;
-  const int64_t nq = static_cast<int64_t>(n_video) + n_text;
+  // The mean key of every resident tile: [heads][T][128] float32.
   const int64_t nc = static_cast<int64_t>(cache->valid_frames) * cache->grid_h * cache->grid_w;
-  const int64_t n_tiles = (nc + 127) / 128, n_groups = (nq + 511) / 512;
-  (void)n_groups;
+  const int64_t n_tiles = (nc + 127) / 128;
   *bytes = round256(static_cast<size_t>(cache->heads) * n_tiles * 128 * 4);
   return NOMAS_OK;
 }

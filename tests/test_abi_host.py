@@ -213,3 +213,20 @@ def test_descriptor_round_trips_through_its_bytes():
                                                ctypes.byref(nt), ctypes.byref(vt)) == nomas.NOMAS_OK
         outs.append((ff.value, sf.value, nt.value, vt.value))
     assert outs[0] == outs[1] == (0, 40 % 18, 48, 18)
+
+
+def test_bench_flop_accounting_is_consistent():
+    # the executed-FLOP counts bench.py reports for block-sparse runs
+    import bench
+    from synth import CONFIGS
+    wl = CONFIGS["c3_int8_window18"]
+    n_t = -(-wl.n_cache // 128)
+    groups = -(-wl.n_q // 512)
+    every = np.tile(np.arange(n_t, dtype=np.int32), (wl.heads, groups, 1))
+    full = np.full((wl.heads, groups), n_t, np.int32)
+    assert bench.sparse_flops(wl, every, full) == wl.attn_flops()
+    none = np.zeros((wl.heads, groups), np.int32)
+    assert bench.sparse_flops(wl, every, none) == 4.0 * wl.n_q * wl.n_q * 128 * wl.heads
+    s5 = CONFIGS["c5_session12"]
+    assert bench.session_flops(s5, 12, keep=1.0) == bench.session_flops(s5, 12)
+    assert bench.session_flops(s5, 12, keep=0.25) < bench.session_flops(s5, 12)
