@@ -9,6 +9,15 @@ the attention's FLOPs (4 * Nq * Nk * 128 * heads) per step time, in TFLOP/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
+The headline workload is the 60-frame BF16 history (``c4_bf16_hist60``, the
+largest single-block call).  The same JSON line carries, under ``configs``, the
+other single-block workloads (the INT8 window of 18 frames and the 8-frame
+BF16 history) measured the same way, and one whole simulated 12-turn session
+(8 denoising steps x 54 blocks per turn), each with attention TFLOP/s, its
+fraction of the measured dense BF16 peak, query tokens per second per block
+call, and the RoPE / append bandwidth against the measured HBM copy rate and
+against 8 TB/s.
+
 Under torchrun (N > 1) every rank runs the same-shaped workload on its own
 seeded data (independent blocks; no collective on the data path) and rank 0
 prints one JSON line with the whole-job throughput (weak scaling).
@@ -25,6 +34,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -33,8 +43,11 @@ if ROOT not in sys.path:
 
 METRIC = "segment-causal KV-cache attention TFLOP/s (% of B300 dense BF16 peak)"
 UNIT = "TFLOP/s"
-DEFAULT_CONFIG = "c2_bf16_hist8"
+DEFAULT_CONFIG = "c4_bf16_hist60"
+EXTRA_CONFIGS = ("c3_int8_window18", "c2_bf16_hist8")
+SESSION_CONFIG = "c5_session12"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+HBM_NOMINAL_GBS = 8000.0  # the "about 8 TB/s" HBM figure the RoPE / append targets are quoted against
 
 
 def load_peaks():
@@ -47,7 +60,7 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -58,6 +71,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads and the session (only the --config workload)")
+    ap.add_argument("--extra-seconds", type=float, default=0.5,
+                    help="timed device time per extra single-block workload (at least --steps steps)")
     ap.add_argument("--turns", type=int, default=12, help="turns of the session workload (c5_session12)")
     ap.add_argument("--cache-dtype", choices=["int8", "fp8", "bf16"], default=None,
                     help="override the config's cache format (fp8: the E4M3 comparison variant)")
@@ -69,7 +86,7 @@ def parse():
                     help="block-sparse attention keeping this fraction of cache tiles (0 = dense)")
     ap.add_argument("--archive", action="store_true",
                     help="session workload: also copy every appended frame to a host archive")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -101,12 +118,37 @@ def whole_job_value(flops_per_step: float, world: int, steps: int, total_ms: flo
     return flops_per_step * world * steps / (total_ms * 1e-3) / 1e12
 
 
+def hbm_entry(nbytes: float, us: float, hbm_gbs: float, launches: int, **extra) -> dict:
+    """Bandwidth summary of an HBM-bound kernel group: algorithmic bytes over its event time."""
+    gbs = nbytes / (us * 1e-6) / 1e9 if us > 0 else None
+    d = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": us, "achieved": gbs, "peak": hbm_gbs,
+         "unit": "GB/s", "frac": gbs / hbm_gbs if gbs else None,
+         "frac_of_8tbs": gbs / HBM_NOMINAL_GBS if gbs else None, "launches_per_step": launches}
+    d.update(extra)
+    return d
+
+
+def append_bytes(wl) -> int:
+    """Algorithmic bytes of the history appends of one step: per written (token, head) row pair, the
+    K and V rows read plus the codes and scales (one-byte caches) or the bf16 rows written."""
+    in_esz = 2 if wl.io_dtype == "bf16" else 4
+    one_byte = wl.cache_dtype in ("int8", "fp8")
+    row = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if one_byte else 2 * wl.head_dim))
+    return sum(min(f, wl.window) for f in wl.cache_frames_hist) * wl.tpf * wl.heads * row
+
+
+def rope_bytes(wl) -> int:
+    """Algorithmic bytes of RoPE of one step: the video rows of Q and K, read and written."""
+    in_esz = 2 if wl.io_dtype == "bf16" else 4
+    return wl.n_video * wl.heads * wl.head_dim * in_esz * 2 * 2
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 def oracle_sample(wl, seconds: float, block: int = 0):
     """Time the oracle's RoPE + segment attention on a sample of query rows.
 
-    Returns (flops_per_second, description, threads).  The sample grows until
-    it takes at least ``seconds`` (capped at the whole segment).
+    Returns (flops_per_second, description, threads, seconds).  The sample
+    grows until it takes at least ``seconds`` (capped at the whole segment).
     """
     import numpy as np
 
@@ -190,72 +232,144 @@ def _config_dict(wl, n_gpus, l2_policy):
             "l2": l2_policy}
 
 
-# ------------------------------------------------------------------ GPU arm
+# ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power, busy % and throttle reasons sampled in a background thread while a timed
+    region runs: NVML every 10 ms (short regions still get samples), else nvidia-smi every 200 ms."""
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, device):
+        self.device = device
         self.proc = None
+        self.thread = None
+        self.stop_flag = threading.Event()
+        self.samples = []   # (sm_mhz, max_mhz, busy_pct, reasons_mask)
+        self.source = None
+        self.nvml_error = None
+
+    def _nvml_handle(self):
+        import pynvml
+        pynvml.nvmlInit()
+        import torch
+        props = torch.cuda.get_device_properties(self.device)
+        tries = []
+        uuid = str(getattr(props, "uuid", ""))
+        if uuid:
+            tries.append(lambda: pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid))
+        if hasattr(props, "pci_bus_id"):
+            bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+            tries.append(lambda: pynvml.nvmlDeviceGetHandleByPciBusId(bus))
+        if pynvml.nvmlDeviceGetCount() == 1 or "CUDA_VISIBLE_DEVICES" not in os.environ:
+            tries.append(lambda: pynvml.nvmlDeviceGetHandleByIndex(self.device.index or 0))
+        errors = []
+        for t in tries:
+            try:
+                return pynvml, t()
+            except Exception as e:  # try the next way of naming the device
+                errors.append(repr(e))
+        raise RuntimeError("no NVML handle: " + "; ".join(errors))
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+            nv, h = self._nvml_handle()
+            smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    try:
+                        sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                        busy = nv.nvmlDeviceGetUtilizationRates(h).gpu
+                        rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                        self.samples.append((float(sm), float(smax), float(busy), int(rs)))
+                    except Exception:
+                        pass
+                    self.stop_flag.wait(0.01)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            self.source = "nvml, 10 ms"
+            return
+        except Exception as e:
+            self.thread = None
+            self.nvml_error = repr(e)[:200]
+        try:
+            idx = self.device.index or 0
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={idx}", f"--query-gpu={self.SMI_FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, 200 ms"
         except OSError:
             self.proc = None
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+        elif self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            names = [n for n, _ in self.REASONS[:4]]
+            for line in out.strip().splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm, smax = float(parts[1]), float(parts[2])
+                except ValueError:
+                    continue
+                mask = 0
+                for (n, bit), v in zip(self.REASONS[:4], parts[5:9]):
+                    if v.lower() == "active":
+                        mask |= bit
+                self.samples.append((sm, smax, 100.0, mask))
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"], "samples": 0}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        loaded = [s for s in self.samples if s[2] >= 50.0] or self.samples
+        reasons = sorted({n for n, bit in self.REASONS for s in loaded if s[3] & bit})
+        out = {"sm_mhz": statistics.median(s[0] for s in loaded), "sm_max_mhz": max(s[1] for s in self.samples),
+               "reasons": reasons, "samples": len(self.samples), "samples_under_load": len(loaded),
+               "source": self.source}
+        if self.nvml_error:
+            out["nvml_error"] = self.nvml_error
+        return out
 
 
-def run_ours(args):
+# ------------------------------------------------------------------ GPU arm: one block call per step
+def _workspace_plan(nomas, cache, wl, num_splits):
+    """Work plan and workspace bytes the library uses once the history is resident."""
+    import ctypes
+    d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
+    total = sum(wl.cache_frames_hist)
+    d.total_frames = total
+    d.valid_frames = min(total, wl.window)
+    pl = nomas.nomas_attn_plan()
+    if nomas.nomas_segment_attn_plan(ctypes.byref(d), wl.n_video, wl.n_text, num_splits, ctypes.byref(pl)) != 0:
+        raise RuntimeError("attention plan query failed")
+    plan = {name: int(getattr(pl, name)) for name, _ in nomas.nomas_attn_plan._fields_ if name != "reserved"}
+    return plan
+
+
+def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=False, target_s=0.0):
+    """Time ``steps`` steps (reset, history append, RoPE, attention [, selection, camera]) of one
+    block call on workload ``wl``; returns raw per-step event timings and the step's accounting.
+    With ``target_s`` the step count grows (up to 1000) until the timed steps take about that long."""
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     import segment_causal_kv_int8_b300 as nomas
-    from synth import CONFIGS, current_qkv, history_segments
+    from synth import current_qkv, history_segments
 
-    rank, world, local = dist_env()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    wl = CONFIGS[args.config]
-    if args.cache_dtype:
-        import dataclasses
-        wl = dataclasses.replace(wl, cache_dtype=args.cache_dtype)
-    block = rank_block(rank)  # each rank owns an independent block's data
-
-    # ---- synthetic inputs (seeded), resident in HBM before timing
     hist = history_segments(wl, block)
     q_h, k_h, v_h = current_qkv(wl, block=block)
 
@@ -269,14 +383,15 @@ def run_ours(args):
                           device=dev)
     lse = torch.empty((wl.heads, wl.n_q), dtype=torch.float32, device=dev)
     out = torch.empty_like(q)
-    ws_bytes, splits_used = _workspace_for(nomas, cache, wl, args.num_splits)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    plan = _workspace_plan(nomas, cache, wl, args.num_splits)
+    ws = torch.empty(max(plan["workspace_bytes"], 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
-    if args.camera:
+    camera = args.camera
+    if camera:
         g = torch.Generator(device=dev)
         g.manual_seed(wl.seed)
-        cam_k = torch.randn((wl.cur_frames, args.camera, wl.heads, wl.head_dim), generator=g, device=dev).to(
+        cam_k = torch.randn((wl.cur_frames, camera, wl.heads, wl.head_dim), generator=g, device=dev).to(
             torch.bfloat16)
         cam_v = torch.randn(cam_k.shape, generator=g, device=dev).to(torch.bfloat16)
         cam_out = torch.empty((wl.n_video, wl.heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
@@ -303,7 +418,7 @@ def run_ours(args):
         flush.view(torch.int32).sum()
 
     def step(ev=None):
-        # ev: None or 8 events bracketing append, RoPE, attention and (sparse) tile selection
+        # ev: None or events bracketing append, RoPE, attention, (sparse) tile selection and camera
         cache.reset(zero_memory=False)
         if ev is not None:
             ev[0].record(stream)
@@ -335,7 +450,7 @@ def run_ours(args):
                                num_splits=args.num_splits)
         if ev is not None:
             ev[5].record(stream)
-        if args.camera:
+        if camera:
             if ev is not None:
                 ev[8].record(stream)
             nomas.camera_cross_attn(q, cam_k, cam_v, wl.cur_frames, wl.grid_h, wl.grid_w, out=cam_out)
@@ -346,109 +461,165 @@ def run_ours(args):
         q.copy_(q0)  # RoPE works in place: fresh un-rotated inputs for every step (untimed)
         k.copy_(k0)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         restage()
         step()
     torch.cuda.synchronize(dev)
+    if target_s > 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        restage()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per = max(1e-6, e0.elapsed_time(e1) * 1e-3)
+        steps = max(steps, min(1000, int(target_s / per)))
+        steps = int(max_over_ranks(steps, world, dev))
 
-    sampler = ClockSampler(dev.index if world == 1 else local)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(args.steps)]
+    import torch.distributed as dist
+    sampler = ClockSampler(dev) if with_sampler else None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.3)
+    if sampler:
+        sampler.start()
+        time.sleep(0.05)
     # Steps are enqueued back to back (one synchronisation after the last).  A
     # GPU-side sleep queued first holds the stream while the host enqueues all
     # steps, so no host launch latency lands between a step's events.  Each
     # step is bracketed by its own events; the L2 flush and the restaging copy
     # sit between steps, outside them, and the sleep precedes the first step.
-    torch.cuda._sleep(int(2e6) * args.steps)
-    for i in range(args.steps):
+    torch.cuda._sleep(int(2e6) * steps)
+    for i in range(steps):
         evict_l2()  # untimed, between steps
         restage()
         evs[i][0].record(stream)
         step(evs[i][2:])
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    append_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    rope_ms = [e[4].elapsed_time(e[5]) for e in evs]
-    attn_ms = [e[6].elapsed_time(e[7]) for e in evs]
-    select_ms = [e[8].elapsed_time(e[9]) for e in evs] if keep else None
-    camera_ms = [e[10].elapsed_time(e[11]) for e in evs] if args.camera else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    clocks = sampler.stop() if sampler else None
+    r = {
+        "step_ms": [e[0].elapsed_time(e[1]) for e in evs],
+        "append_ms": [e[2].elapsed_time(e[3]) for e in evs],
+        "rope_ms": [e[4].elapsed_time(e[5]) for e in evs],
+        "attn_ms": [e[6].elapsed_time(e[7]) for e in evs],
+        "select_ms": [e[8].elapsed_time(e[9]) for e in evs] if keep else None,
+        "camera_ms": [e[10].elapsed_time(e[11]) for e in evs] if camera else None,
+        "clocks": clocks, "plan": plan, "hist": hist, "qkv": (q_h, k_h, v_h), "steps": steps,
+    }
+    r["flops"] = sparse_flops(wl, sel_tiles.cpu().numpy(), sel_counts.cpu().numpy()) if keep else wl.attn_flops()
+    r["launches_per_step"] = (len(hist) + 1 + 1 + (1 if plan["pieces_per_split_unit"] > 1 else 0)
+                              + (2 if keep and wl.n_cache else 0) + (1 if camera else 0))
+    del cache, hist_d, flush, ws
+    return r
+
+
+def summarize_block_call(wl, m, world, steps, peaks, append_rope=False, camera=0):
+    """Per-workload summary: attention TFLOP/s and roofline fractions, query tokens/s, step time,
+    RoPE and append bandwidth (fractions of the measured copy rate and of 8 TB/s)."""
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    attn_avg = statistics.mean(m["attn_ms"])
+    step_avg = statistics.mean(m["step_ms"])
+    achieved = m["flops"] / (attn_avg * 1e-3) / 1e12
+    el = {}
+    name = "kvcache_append_rope" if append_rope else "kvcache_append"
+    el[name] = hbm_entry(append_bytes(wl), 1e3 * statistics.mean(m["append_ms"]), hbm, len(wl.cache_frames_hist))
+    el["rope3d"] = hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_ms"]), hbm, 1)
+    if camera:
+        nbytes = 2 * wl.n_video * wl.heads * wl.head_dim * 2 + 2 * wl.cur_frames * camera * wl.heads * wl.head_dim * 2
+        el["camera_cross_attn"] = hbm_entry(nbytes, 1e3 * statistics.mean(m["camera_ms"]), hbm, 1,
+                                            camera_tokens_per_frame=camera)
+    return {
+        "workload": _config_dict(wl, world, "")["workload"],
+        "attention": {"tflops": achieved, "frac": achieved / peak, "frac_of_sustained": achieved / peak_s,
+                      "us": 1e3 * attn_avg, "q_tokens_per_s": wl.n_q / (attn_avg * 1e-3),
+                      "plan": m["plan"]},
+        "step": {"ms": step_avg, "tflops": m["flops"] / (step_avg * 1e-3) / 1e12,
+                 "q_tokens_per_s": wl.n_q / (step_avg * 1e-3), "steps": steps},
+        "elementwise": el,
+    }
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import segment_causal_kv_int8_b300 as nomas
+    from synth import CONFIGS
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    wl = CONFIGS[args.config]
+    if args.cache_dtype:
+        import dataclasses
+        wl = dataclasses.replace(wl, cache_dtype=args.cache_dtype)
+    block = rank_block(rank)  # each rank owns an independent block's data
+    peaks, src = load_peaks()
+
+    m = measure_block_call(args, wl, dev, block, args.steps, args.warmup, world, with_sampler=True)
+    total_ms = max_over_ranks(sum(m["step_ms"]), world, dev)
     ms_per_step = total_ms / args.steps
-    flops = wl.attn_flops()
-    if keep:
-        flops = sparse_flops(wl, sel_tiles.cpu().numpy(), sel_counts.cpu().numpy())
+    flops = m["flops"]
     value = whole_job_value(flops, world, args.steps, total_ms)
-    attn_avg = statistics.mean(attn_ms)
-    achieved = flops / (attn_avg * 1e-3) / 1e12
+    keep = args.sparse
+    summary = summarize_block_call(wl, m, world, args.steps, peaks, args.append_rope, args.camera)
+    att = summary["attention"]
 
     e2e = None
     if not args.no_e2e and not keep and not args.append_rope:
-        e2e = _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world)
+        e2e = _e2e(args, torch, nomas, wl, m["hist"], *m["qkv"], dev, world)
+    m["hist"] = m["qkv"] = None
 
-    launches_per_step = (len(hist) + 1 + 1 + (1 if splits_used > 1 else 0) + (2 if keep and wl.n_cache else 0)
-                         + (1 if args.camera else 0))
-    peaks, src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    in_esz = 2 if wl.io_dtype == "bf16" else 4
-    rope_bytes = wl.n_video * wl.heads * wl.head_dim * in_esz * 2 * 2  # Q and K, read + write
-    row_bytes = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if wl.cache_dtype in ("int8", "fp8") else 2 * wl.head_dim))
-    append_bytes = sum(min(f, wl.window) for f in wl.cache_frames_hist) * wl.tpf * wl.heads * row_bytes
-    elementwise = {}
-    append_name = "kvcache_append_rope" if args.append_rope else "kvcache_append"
-    for name, nbytes, ms in ((append_name, append_bytes, append_ms), ("rope3d", rope_bytes, rope_ms)):
-        t = statistics.mean(ms)
-        gbs = nbytes / (t * 1e-3) / 1e9 if t > 0 else None
-        elementwise[name] = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": 1e3 * t, "achieved": gbs,
-                             "peak": hbm, "unit": "GB/s", "frac": gbs / hbm if gbs else None,
-                             "launches_per_step": len(hist) if name == append_name else 1}
-    # the committed counters describe the config's own cache format
-    if args.camera:
-        t = statistics.mean(camera_ms)
-        nbytes = 2 * wl.n_video * wl.heads * wl.head_dim * 2 + 2 * wl.cur_frames * args.camera * wl.heads * wl.head_dim * 2
-        gbs = nbytes / (t * 1e-3) / 1e9 if t > 0 else None
-        elementwise["camera_cross_attn"] = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": 1e3 * t,
-                                            "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                                            "frac": gbs / hbm if gbs else None, "launches_per_step": 1,
-                                            "camera_tokens_per_frame": args.camera}
-    traffic = _load_traffic(args.config) if wl.cache_dtype == CONFIGS[args.config].cache_dtype else None
+    configs = {}
+    if not args.no_extras and not keep and not args.append_rope and not args.camera and not args.cache_dtype:
+        configs = run_extras(args, wl, dev, world, peaks)
+
+    traffic, traffic_source = _load_traffic(args.config)
+    if wl.cache_dtype != CONFIGS[args.config].cache_dtype or keep:
+        traffic, traffic_source = None, "not captured for this variant"
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": _config_dict(wl, world, "256 MiB buffer written then read between timed steps (L2 flush, untimed)"),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "segment_attn_kernel" + (" + combine" if splits_used > 1 else ""),
-                         "attn_ms": attn_avg, "splits": splits_used,
+            "roofline": {"bound": "tensor", "achieved": att["tflops"], "peak": float(peaks.get("bf16_tflops", 0)),
+                         "unit": UNIT, "frac": att["frac"], "frac_of_sustained": att["frac_of_sustained"],
+                         "traffic": traffic, "traffic_source": traffic_source,
+                         "kernel": "segment_attn_kernel" + (" + combine" if m["plan"]["pieces_per_split_unit"] > 1
+                                                            else ""),
+                         "attn_ms": att["us"] / 1e3, "plan": m["plan"],
                          "peak_source": f"bf16_tflops (burst) of {src} peaks"},
-            "elementwise": elementwise,
+            "q_tokens_per_s": att["q_tokens_per_s"],
+            "q_tokens_per_s_step": summary["step"]["q_tokens_per_s"],
+            "elementwise": summary["elementwise"],
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks,
+            "gpu_launches": m["launches_per_step"] * args.steps,
+            "clocks": m["clocks"],
         }
+        if configs:
+            line["configs"] = configs
         if args.append_rope:
             line["config"]["workload"] += "; history written by the fused RoPE + append"
         if keep:
             # Executed FLOPs count each query group's kept keys; the dense
             # equivalent is the full-attention FLOPs over the same step time.
             line["config"]["workload"] += f"; block-sparse, keep {keep} of the cache tiles"
-            line["sparse"] = {"keep": keep, "select_us": 1e3 * statistics.mean(select_ms),
+            line["sparse"] = {"keep": keep, "select_us": 1e3 * statistics.mean(m["select_ms"]),
                               "executed_flops": flops, "dense_flops": wl.attn_flops(),
                               "dense_equivalent_tflops": whole_job_value(wl.attn_flops(), world, args.steps,
                                                                          total_ms)}
             line["roofline"]["kernel"] += " (tile lists)"
-            line["roofline"]["traffic"] = None
         if not args.no_cpu_baseline and world == 1:
             v_cpu, desc, threads, _ = oracle_sample(wl, args.cpu_seconds)
             line["cpu_baseline"] = {"value": v_cpu / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -457,6 +628,38 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_extras(args, main_wl, dev, world, peaks):
+    """The other single-block workloads (timed like the headline, at least --steps steps and about
+    --extra-seconds of device time each) and one whole session, for the ``configs`` key."""
+    import torch
+
+    from synth import CONFIGS
+
+    rank, _, _ = dist_env()
+    out = {}
+    for name in EXTRA_CONFIGS:
+        if name == main_wl.name:
+            continue
+        wl = CONFIGS[name]
+        m = measure_block_call(args, wl, dev, rank_block(rank), args.steps, max(3, args.warmup), world,
+                               with_sampler=True, target_s=args.extra_seconds)
+        steps = m["steps"]
+        m["hist"] = m["qkv"] = None
+        total = max_over_ranks(sum(m["step_ms"]), world, dev)
+        s = summarize_block_call(wl, m, world, steps, peaks)
+        s["step"]["ms"] = total / steps
+        s["step"]["whole_job_tflops"] = whole_job_value(m["flops"], world, steps, total)
+        s["clocks"] = m["clocks"]
+        s["gpu_launches"] = m["launches_per_step"] * steps
+        out[name] = s
+        torch.cuda.empty_cache()
+    sess = measure_session(args, CONFIGS[SESSION_CONFIG], dev, world, rank, args.turns, steps=1, warmup=[1],
+                           keep=0.0, archive=False)
+    out[SESSION_CONFIG] = session_summary(CONFIGS[SESSION_CONFIG], sess, world, peaks)
+    torch.cuda.empty_cache()
+    return out
 
 
 def sparse_flops(wl, tiles, counts) -> float:
@@ -470,25 +673,14 @@ def sparse_flops(wl, tiles, counts) -> float:
     return total
 
 
-def _workspace_for(nomas, cache, wl, num_splits):
-    """Workspace bytes and split count the library uses once the history is resident."""
-    import ctypes
-    d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
-    total = sum(wl.cache_frames_hist)
-    d.total_frames = total
-    d.valid_frames = min(total, wl.window)
-    b = ctypes.c_size_t()
-    st = nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), wl.n_video, wl.n_text, num_splits,
-                                                  ctypes.byref(b))
-    if st != 0:
-        raise RuntimeError("workspace query failed")
-    if b.value == 0:
-        return 0, 1
-    return int(b.value), max(2, int(b.value // (wl.heads * wl.n_q * 128 * 4)))
-
-
 def _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world):
-    """Same step through the public API with host (pinned) inputs and a host read of the output."""
+    """Same step through the public API with host (pinned) inputs and a host read of the output.
+
+    ``value``: the whole step (history segments, Q, K, V uploaded every step).
+    ``per_call_resident_cache``: the pages' serving pattern, where the cache
+    stays resident between calls and each block call uploads only the current
+    segment's Q, K, V and reads back O (RoPE + attention per call).
+    """
     import torch.distributed as dist
 
     def pin(x, bf16):
@@ -503,44 +695,69 @@ def _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world):
     qd, kd, vd = (torch.empty_like(x, device=dev) for x in (qh, kh, vh))
     cache = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames, wl.cache_dtype,
                           device=dev)
-    ws_bytes, _ = _workspace_for(nomas, cache, wl, args.num_splits)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    plan = _workspace_plan(nomas, cache, wl, args.num_splits)
+    ws = torch.empty(max(plan["workspace_bytes"], 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(qd)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    h2d = sum(a.numel() * a.element_size() * 2 for a, _ in hist_h) + 3 * qh.numel() * qh.element_size()
+    qkv_bytes = 3 * qh.numel() * qh.element_size()
+    h2d = sum(a.numel() * a.element_size() * 2 for a, _ in hist_h) + qkv_bytes
     d2h = out_h.numel() * out_h.element_size()
 
-    def step():
-        for (a, b), (ad, bd) in zip(hist_h, hist_d):
-            ad.copy_(a, non_blocking=True)
-            bd.copy_(b, non_blocking=True)
+    def upload_qkv():
         for x, xd in ((qh, qd), (kh, kd), (vh, vd)):
             xd.copy_(x, non_blocking=True)
-        cache.reset(zero_memory=False)
-        for ad, bd in hist_d:
-            cache.append(ad, bd)
+
+    def block_call():
         nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
         nomas.segment_attn(cache, 0, qd, kd, vd, wl.n_video, wl.n_text, out=out, workspace=ws,
                            num_splits=args.num_splits)
         out_h.copy_(out, non_blocking=True)
 
+    def step():
+        for (a, b), (ad, bd) in zip(hist_h, hist_d):
+            ad.copy_(a, non_blocking=True)
+            bd.copy_(b, non_blocking=True)
+        upload_qkv()
+        cache.reset(zero_memory=False)
+        for ad, bd in hist_d:
+            cache.append(ad, bd)
+        block_call()
+
+    def timed(fn, n):
+        ms = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return ms
+
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
-    ms = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms.append(e0.elapsed_time(e1))
-    total = max_over_ranks(sum(ms), world, dev)
+    if world > 1:
+        dist.barrier()
+    total = max_over_ranks(sum(timed(step, args.steps)), world, dev)
     val = whole_job_value(wl.attn_flops(), world, args.steps, total)
-    return {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": total / args.steps}
+
+    def per_call():
+        upload_qkv()
+        block_call()
+
+    per_call()  # the cache now holds the history (resident from the last step); warm the path
+    torch.cuda.synchronize(dev)
+    total_pc = max_over_ranks(sum(timed(per_call, args.steps)), world, dev)
+    res = {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "ms_per_step": total / args.steps,
+           "per_call_resident_cache": {"value": whole_job_value(wl.attn_flops(), world, args.steps, total_pc),
+                                       "unit": UNIT, "ms_per_call": total_pc / args.steps,
+                                       "h2d_bytes_per_call": int(qkv_bytes), "d2h_bytes_per_call": int(d2h)}}
+    del cache, hist_d, ws, flush
+    return res
 
 
 ATTN_SOURCES = ("segment_causal_kv_int8_b300/csrc/segment_attn.cu", "segment_causal_kv_int8_b300/csrc/sm100.cuh")
@@ -559,26 +776,28 @@ def attn_source_hash() -> str:
 def _load_traffic(config):
     """DRAM bytes per attention launch from the committed ncu summary of this config.
 
-    ``profiles/attention_<config>.md`` records ``dram_bytes_per_launch`` and the
-    ``kernel_source_sha256`` of the sources it was captured from; the value is
-    used only while the sources still hash the same, else traffic is null.
+    ``profiles/attention_<config>.md`` records ``dram_bytes_per_launch`` (an
+    ncu capture of that launch) and the ``kernel_source_sha256`` of the sources
+    it was captured from; the value is used only while the sources still hash
+    the same.  Returns ``(bytes or None, description of the source)``.
     """
-    path = os.path.join(ROOT, "profiles", f"attention_{config}.md")
+    rel = os.path.join("profiles", f"attention_{config}.md")
     fields = {}
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, rel)) as f:
             for line in f:
                 if ":" in line:
                     k, _, v = line.strip().lstrip("-* `").partition(":")
                     fields[k.strip(" `")] = v.strip(" `")
     except OSError:
-        return None
+        return None, f"no ncu capture committed ({rel} missing)"
     if fields.get("kernel_source_sha256") != attn_source_hash():
-        return None
+        return None, f"{rel} was captured from other kernel sources (hash differs)"
     try:
-        return int(float(fields["dram_bytes_per_launch"]))
+        return int(float(fields["dram_bytes_per_launch"])), (
+            f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, {rel} (same kernel sources)")
     except (KeyError, ValueError):
-        return None
+        return None, f"{rel} holds no dram_bytes_per_launch"
 
 
 # ------------------------------------------------------------------ session workload
@@ -606,24 +825,20 @@ def session_flops(wl, turns: int, keep: float = 0.0, dense_steps: int = 2) -> fl
     return total
 
 
-def run_session(args):
-    """The simulated multi-turn session: per turn, steps x blocks calls of RoPE + segment attention
-    (each block against its own window of the shared INT8 cache), then one append of the finished
-    segment's K/V for all blocks.  One timed step = one whole session of ``--turns`` turns."""
+def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, archive):
+    """Time ``steps`` whole sessions of ``turns`` turns: per turn, steps x blocks calls of RoPE +
+    segment attention (each block against its own window of the shared INT8 cache), then one append
+    of the finished segment's K/V for all blocks.  ``warmup`` lists the turn counts of the untimed
+    sessions run first."""
+    import ctypes
+
     import torch
     import torch.distributed as dist
 
     import segment_causal_kv_int8_b300 as nomas
-    from synth import CONFIGS, current_qkv_torch, segment_kv_torch
+    from synth import current_qkv_torch, segment_kv_torch
 
-    rank, world, local = dist_env()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    wl = CONFIGS[args.config]
-    turns = min(args.turns, wl.turns)
+    turns = min(turns, wl.turns)
     seed_block = rank_block(rank)
     cache = nomas.KVCache(wl.blocks, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames,
                           wl.cache_dtype, device=dev)
@@ -636,14 +851,12 @@ def run_session(args):
     for vf in range(0, wl.window + 1):
         d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
         d.total_frames, d.valid_frames = vf, vf
-        import ctypes
         b = ctypes.c_size_t()
         nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), wl.n_video, wl.n_text, 0, ctypes.byref(b))
         ws_bytes = max(ws_bytes, int(b.value))
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     calls = [0]
-    keep = args.sparse
     if keep:
         # Block-sparse after two dense steps: per block a kept-tile list and
         # the mean keys of its window (computed at the first sparse step of a
@@ -655,15 +868,18 @@ def run_session(args):
         sel_counts = torch.zeros((wl.heads, groups), dtype=torch.int32, device=dev)
         kbar_bytes = -(-wl.heads * n_tiles_max * 128 * 4 // 256) * 256
         kbar = torch.empty((wl.blocks, kbar_bytes), dtype=torch.uint8, device=dev)
-    archive = None
-    if args.archive:
+    host_archive = None
+    if archive:
         # Host KV archive of every appended frame (pinned, one session's worth).
-        archive = torch.empty(turns * wl.cur_frames * cache.archive_frame_bytes(), dtype=torch.uint8).pin_memory()
+        host_archive = torch.empty(turns * wl.cur_frames * cache.archive_frame_bytes(),
+                                   dtype=torch.uint8).pin_memory()
 
-    def session():
+    def session(n_turns):
         cache.reset(zero_memory=False)
         used = 0
-        for t in range(turns):
+        for t in range(n_turns):
+            # the plan (and so whether a merge pass follows) depends on the resident frames
+            merge = 1 if cache.attn_plan(wl.n_video, wl.n_text)["pieces_per_split_unit"] > 1 else 0
             for s in range(wl.steps):
                 for blk in range(wl.blocks):
                     q, k, v = pool[(s * wl.blocks + blk) % len(pool)]
@@ -677,35 +893,73 @@ def run_session(args):
                         calls[0] += 3 + (1 if s == 2 else 0)
                     else:
                         nomas.segment_attn(cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
-                        calls[0] += 1
+                        calls[0] += 1 + merge
                     calls[0] += 1
-            if archive is not None:
-                used = cache.append_archive(seg_k, seg_v, archive, used)
+            if host_archive is not None:
+                used = cache.append_archive(seg_k, seg_v, host_archive, used)
             else:
                 cache.append(seg_k, seg_v)
             calls[0] += 1
 
-    for _ in range(args.warmup):
-        session()
+    for n in warmup:
+        session(min(n, turns))
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler = ClockSampler(dev)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.start()
-    time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    time.sleep(0.05)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     calls[0] = 0
-    for i in range(args.steps):
+    for i in range(steps):
         evs[i][0].record(stream)
-        session()
+        session(turns)
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
-    flops = session_flops(wl, turns, keep)
+    del cache, ws, pool
+    return {"total_ms": total_ms, "steps": steps, "turns": turns, "calls": calls[0], "clocks": clocks,
+            "flops": session_flops(wl, turns, keep), "keep": keep, "archive": archive}
+
+
+def session_summary(wl, s, world, peaks):
+    peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tf = whole_job_value(s["flops"], world, s["steps"], s["total_ms"]) / world
+    calls = s["turns"] * wl.steps * wl.blocks
+    return {"workload": f"{wl.name}: {s['turns']} turns x {wl.steps} steps x {wl.blocks} blocks of RoPE + segment "
+                        f"attention (Nq={wl.n_q}, INT8 window {wl.window} frames), one 54-block append per turn",
+            "session_s": s["total_ms"] / s["steps"] / 1e3, "attention_calls": calls,
+            "tflops": tf, "frac_of_sustained": tf / peak_s,
+            "q_tokens_per_s": calls * wl.n_q / (s["total_ms"] / s["steps"] / 1e3),
+            "peak": peak_s, "peak_source": "bf16_tflops_sustained (a seconds-long step)",
+            "gpu_launches": s["calls"], "clocks": s["clocks"]}
+
+
+def run_session(args):
+    """The simulated multi-turn session as the headline workload (``--config c5_session12``):
+    one timed step = one whole session of ``--turns`` turns."""
+    import torch
+    import torch.distributed as dist
+
+    from synth import CONFIGS
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    wl = CONFIGS[args.config]
+    keep = args.sparse
+    s = measure_session(args, wl, dev, world, rank, args.turns, args.steps, [args.turns] * args.warmup, keep,
+                        args.archive)
+    turns = s["turns"]
+    total_ms = s["total_ms"]
+    flops = s["flops"]
     value = whole_job_value(flops, world, args.steps, total_ms)
     peaks, src = load_peaks()
     if rank == 0:
@@ -722,9 +976,11 @@ def run_session(args):
                        "parallelism": f"replica x{world} (independent sessions per GPU)"},
             "roofline": {"bound": "tensor", "achieved": value / world, "peak": float(peaks["bf16_tflops_sustained"]),
                          "unit": UNIT, "frac": value / world / float(peaks["bf16_tflops_sustained"]),
-                         "traffic": None, "kernel": "whole session (attention dominant)",
+                         "traffic": None, "traffic_source": "not captured (thousands of launches per step)",
+                         "kernel": "whole session (attention dominant)",
                          "peak_source": f"bf16_tflops_sustained of {src} peaks (a seconds-long step)"},
-            "gpu_launches": calls[0], "clocks": clocks,
+            "q_tokens_per_s": turns * wl.steps * wl.blocks * wl.n_q * args.steps / (total_ms * 1e-3),
+            "gpu_launches": s["calls"], "clocks": s["clocks"],
         }
         if keep:
             line["config"]["workload"] += (f"; steps 0-1 dense, steps 2-{wl.steps - 1} block-sparse keeping {keep} "
@@ -743,7 +999,7 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
-    if args.config == "c5_session12":
+    if args.config == SESSION_CONFIG:
         return run_session(args)
     return run_ours(args)
 

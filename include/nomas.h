@@ -222,12 +222,42 @@ nomas_status nomas_kvcache_append_archive(nomas_kvcache* cache, const void* k, c
                                           size_t archive_bytes, size_t* archive_used, cudaStream_t stream);
 
 /*
- * Scratch bytes nomas_segment_attn needs for a given split count (0 = the
- * split count it would choose itself).  Host only.
+ * How nomas_segment_attn divides its work.  A unit is one head x one block of
+ * 256 query rows (BF16 cache, one CTA) or one head x two adjacent blocks (INT8
+ * and FP8 caches, a pair of CTAs that share every dequantised key tile); units
+ * are ordered head by head.  The first whole_units units run whole; every
+ * later unit is cut into pieces_per_split_unit pieces of its key range, whose
+ * partial outputs a second kernel merges in piece order.
+ *
+ *   num_splits = 0   automatic: the whole units fill the full waves of the
+ *                    device's SMs and only the units of the last, partial wave
+ *                    are cut (so they end together), or nothing is cut, or
+ *                    every unit is, whichever a cost model of waves, per-unit
+ *                    fixed cost and merge traffic finds cheapest
+ *   num_splits = 1   nothing is cut
+ *   num_splits = s   every unit is cut into s pieces (at most the number of
+ *                    key tiles of 128 keys, and 64)
+ *
+ * nomas_segment_attn_workspace_bytes: device scratch the plan needs (0 when
+ * nothing is cut): float32 partial outputs and log-sum-exps of every piece.
+ * nomas_segment_attn_plan: the plan itself.  Both host only; for num_splits =
+ * 0 they read the current device's SM count.
  */
+typedef struct {
+  int32_t units;                  /* heads x query units                         */
+  int32_t whole_units;            /* units run whole                             */
+  int32_t pieces_per_split_unit;  /* pieces of every later unit (1 = none cut)   */
+  int32_t ctas_per_unit;          /* 1 (BF16 cache) or 2 (one-byte caches)        */
+  int32_t work_items;             /* whole units + pieces                        */
+  int32_t reserved;
+  size_t workspace_bytes;         /* as nomas_segment_attn_workspace_bytes        */
+} nomas_attn_plan;
+
 nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int32_t n_video,
                                                 int32_t n_text, int32_t num_splits,
                                                 size_t* bytes);
+nomas_status nomas_segment_attn_plan(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
+                                     int32_t num_splits, nomas_attn_plan* plan);
 
 /*
  * Segment attention of one block (the "segment-wise causal joint attention"
@@ -241,17 +271,38 @@ nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int3
  *   out              device bf16 [n_video + n_text][heads][head_dim]
  *   lse              device float32 [heads][n_video + n_text] (natural log), or NULL
  *   workspace        device scratch of workspace_bytes (see
- *                    nomas_segment_attn_workspace_bytes), or NULL/0: the key
- *                    range is then processed in one split
- *   num_splits       key-range splits (0 = automatic); more than 1 needs workspace
+ *                    nomas_segment_attn_workspace_bytes), 256-byte aligned, or
+ *                    NULL/0: with num_splits = 0 nothing is then cut
+ *   num_splits       0 = automatic plan, 1 = none cut, s > 1 = every unit in s
+ *                    pieces (see nomas_segment_attn_plan); s > 1 without enough
+ *                    workspace is NOMAS_ERR_INVALID_ARG
  * BF16 tensor-core products with float32 accumulation and float32 softmax.
- * Results are bitwise reproducible for a given split count.
+ * Results are bitwise reproducible for a given plan (num_splits on the same
+ * device model).
  */
 nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t block, const void* q,
                                 const void* k_cur, const void* v_cur, int32_t n_video,
                                 int32_t n_text, float softmax_scale, void* out, float* lse,
                                 void* workspace, size_t workspace_bytes, int32_t num_splits,
                                 cudaStream_t stream);
+
+/*
+ * nomas_segment_attn with a caller-chosen work plan (for example one tuned
+ * for another SM count, or a fixed plan kept across devices for bitwise
+ * reproducibility).  plan->units and plan->ctas_per_unit must equal what
+ * nomas_segment_attn_plan reports for these arguments; 0 <= whole_units <=
+ * units; 1 <= pieces_per_split_unit <= min(key tiles, 64) (ignored when
+ * whole_units = units).  The workspace must hold what such a plan needs:
+ * (units - whole_units) x pieces x ctas_per_unit x 256 rows of 516 bytes, each
+ * of the two arrays rounded up to 256 bytes.  Anything else returns
+ * NOMAS_ERR_INVALID_ARG without a launch.  Other arguments as
+ * nomas_segment_attn.
+ */
+nomas_status nomas_segment_attn_planned(const nomas_kvcache* cache, int32_t block, const void* q,
+                                        const void* k_cur, const void* v_cur, int32_t n_video,
+                                        int32_t n_text, float softmax_scale, void* out, float* lse,
+                                        void* workspace, size_t workspace_bytes,
+                                        const nomas_attn_plan* plan, cudaStream_t stream);
 
 /*
  * Block-sparse segment attention.  The single-GPU preset of the RTX 4090
@@ -331,10 +382,12 @@ nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int32_t block
  * has reserved nearly all of HBM for its own pools, or a latency-bound loop
  * that cannot accept an allocation's implicit synchronisation).
  *
- * Arguments as nomas_segment_attn.  Returns NOMAS_ERR_CAPACITY, launching
- * nothing, when the split count asked for (or chosen automatically for
- * num_splits = 0) needs more scratch than NOMAS_NOALLOC_SCRATCH_BYTES;
- * nomas_segment_attn_workspace_bytes gives the need.  Every call shares the
+ * Arguments as nomas_segment_attn.  With num_splits = 0 the automatic plan is
+ * used when its scratch fits; otherwise its split units are cut into fewer
+ * pieces, down to none, until it fits, so the call always runs.  An explicit
+ * num_splits > 1 whose scratch exceeds NOMAS_NOALLOC_SCRATCH_BYTES returns
+ * NOMAS_ERR_CAPACITY and launches nothing (nomas_segment_attn_workspace_bytes
+ * gives the need).  Every call shares the
  * array and it keeps the last call's contents (nothing in it must start at
  * zero); calls whose kernels overlap on the GPU race on it.  The first call on
  * a device looks up the array's address with that device current, so make it

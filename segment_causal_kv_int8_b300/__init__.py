@@ -64,6 +64,20 @@ class nomas_kvcache(ctypes.Structure):
     ]
 
 
+class nomas_attn_plan(ctypes.Structure):
+    """Mirror of the C ``nomas_attn_plan`` (how nomas_segment_attn divides its work)."""
+
+    _fields_ = [
+        ("units", ctypes.c_int32),
+        ("whole_units", ctypes.c_int32),
+        ("pieces_per_split_unit", ctypes.c_int32),
+        ("ctas_per_unit", ctypes.c_int32),
+        ("work_items", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 _P = ctypes.POINTER
 _c_int, _i32, _i64, _f32, _vp, _sz = (ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                       ctypes.c_void_p, ctypes.c_size_t)
@@ -84,8 +98,11 @@ EXPORTS = {
     "nomas_kvcache_append_archive": (_c_int, [_P(nomas_kvcache), _vp, _vp, _c_int, _i32, _i64, _vp, _sz, _P(_sz),
                                               _vp]),
     "nomas_segment_attn_workspace_bytes": (_c_int, [_P(nomas_kvcache), _i32, _i32, _i32, _P(_sz)]),
+    "nomas_segment_attn_plan": (_c_int, [_P(nomas_kvcache), _i32, _i32, _i32, _P(nomas_attn_plan)]),
     "nomas_segment_attn": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
                                     _sz, _i32, _vp]),
+    "nomas_segment_attn_planned": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
+                                            _vp, _sz, _P(nomas_attn_plan), _vp]),
     "nomas_segment_attn_noalloc": (_c_int, [_P(nomas_kvcache), _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp,
                                             _i32, _vp]),
     "nomas_sparse_select_workspace_bytes": (_c_int, [_P(nomas_kvcache), _i32, _i32, _P(_sz)]),
@@ -265,6 +282,13 @@ class KVCache:
         _check(nomas_kvcache_reset(ctypes.byref(self.desc), int(bool(zero_memory)), _stream_ptr(stream)),
                "nomas_kvcache_reset")
 
+    def attn_plan(self, n_video: int, n_text: int, num_splits: int = 0) -> dict:
+        """The work plan nomas_segment_attn runs for these arguments (see ``nomas_segment_attn_plan``)."""
+        pl = nomas_attn_plan()
+        _check(nomas_segment_attn_plan(ctypes.byref(self.desc), n_video, n_text, num_splits, ctypes.byref(pl)),
+               "nomas_segment_attn_plan")
+        return {name: int(getattr(pl, name)) for name, _ in nomas_attn_plan._fields_ if name != "reserved"}
+
     def workspace_bytes(self, n_video: int, n_text: int, num_splits: int = 0) -> int:
         out = ctypes.c_size_t(0)
         _check(nomas_segment_attn_workspace_bytes(ctypes.byref(self.desc), n_video, n_text, num_splits,
@@ -298,6 +322,37 @@ def segment_attn(cache: KVCache, block: int, q, k_cur, v_cur, n_video: int, n_te
                               softmax_scale, ctypes.c_void_p(out.data_ptr()),
                               ctypes.c_void_p(lse.data_ptr() if lse is not None else 0), ctypes.c_void_p(ws_ptr),
                               ws_bytes, num_splits, _stream_ptr(stream)), "nomas_segment_attn")
+    return out
+
+
+def plan_workspace_bytes(units: int, whole_units: int, pieces: int, ctas_per_unit: int) -> int:
+    """Scratch bytes of a work plan (float32 partial rows and log-sum-exps of every piece)."""
+    rows = (units - whole_units) * pieces * ctas_per_unit * 256 if pieces > 1 and whole_units < units else 0
+    return -(-rows * 512 // 256) * 256 + -(-rows * 4 // 256) * 256
+
+
+def segment_attn_planned(cache: KVCache, block: int, q, k_cur, v_cur, n_video: int, n_text: int,
+                         whole_units: int, pieces: int, softmax_scale: Optional[float] = None, out=None, lse=None,
+                         workspace=None, stream=None):
+    """Segment attention with a caller-chosen plan: the first ``whole_units`` units whole, the rest in
+    ``pieces`` pieces each (see ``nomas_segment_attn_planned``); allocates the workspace when not given."""
+    torch = _torch()
+    base = cache.attn_plan(n_video, n_text, 1)
+    pl = nomas_attn_plan(base["units"], whole_units, pieces, base["ctas_per_unit"], 0, 0, 0)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        need = plan_workspace_bytes(base["units"], whole_units, pieces, base["ctas_per_unit"])
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[2])
+    _check(nomas_segment_attn_planned(ctypes.byref(cache.desc), block, ctypes.c_void_p(q.data_ptr()),
+                                      ctypes.c_void_p(k_cur.data_ptr()), ctypes.c_void_p(v_cur.data_ptr()), n_video,
+                                      n_text, softmax_scale, ctypes.c_void_p(out.data_ptr()),
+                                      ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                                      ctypes.c_void_p(workspace.data_ptr()),
+                                      workspace.numel() * workspace.element_size(), ctypes.byref(pl),
+                                      _stream_ptr(stream)), "nomas_segment_attn_planned")
     return out
 
 
@@ -420,7 +475,7 @@ def device_error(clear: bool = True) -> int:
     return int(st.value)
 
 
-__all__ = ["KVCache", "rope3d", "segment_attn", "sparse_select", "segment_attn_sparse", "sparse_keep_count",
+__all__ = ["KVCache", "rope3d", "segment_attn", "segment_attn_planned", "plan_workspace_bytes", "sparse_select", "segment_attn_sparse", "sparse_keep_count",
            "camera_cross_attn",
-           "device_error", "NomasError", "nomas_kvcache", "EXPORTS",
+           "device_error", "NomasError", "nomas_kvcache", "nomas_attn_plan", "EXPORTS",
            "LIB_PATH"] + list(EXPORTS)

@@ -27,6 +27,8 @@ struct RopeParams {
   int tpf;                       // grid_h * grid_w
   int grid_w;
   long long t0;
+  long long extent;              // elements of Q (and K) the call may touch (checked build)
+  uint32_t* err;                 // device error word (checked build)
 };
 
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream);
@@ -49,7 +51,9 @@ struct AppendParams {
   float* ks;                     // scales (int8 only)
   float* vs;
   int chunk_tokens;              // staged kernel: tokens per bulk-loaded chunk
-  uint32_t* err;                 // device error word (staged kernel's bounded waits)
+  uint32_t* err;                 // device error word (staged kernel's bounded waits; checked build)
+  long long src_extent;          // elements of each input tensor (checked build)
+  long long cache_rows;          // blocks * heads * cap_slots rows of each cache tensor (checked build)
 };
 
 cudaError_t launch_append(bool f32_in, int kind, const AppendParams& p, int sms, cudaStream_t stream);
@@ -107,19 +111,28 @@ struct AttnTensorMaps {
   CUtensorMap q, kcur, vcur, kc, vc;
 };
 
+// Work plan of one attention call.  A unit is one head x one block of 256
+// query rows (BF16 cache) or one head x two adjacent such blocks (one-byte
+// caches, whose CTA pairs share every dequantised tile), units ordered head
+// by head.  Work items 0 .. n_full-1 are whole units (item i = unit i); every
+// later unit is cut into tail_splits pieces of its key-tile range, whose
+// partial outputs a combine pass merges in piece order.  With n_full = all
+// units nothing is split; with n_full = 0 every unit is split evenly.
 struct AttnParams {
   int nq;                        // current-segment tokens (queries and current keys)
   int nc;                        // resident cache tokens
   int heads;
   int n_cache_tiles;             // ceil(nc / 128)
   int n_cur_tiles;               // ceil(nq / 128)
-  int num_splits;
+  int units_per_head;            // query units per head
+  int n_full;                    // whole-unit work items
+  int tail_splits;               // pieces per unit after the whole ones (1 = none)
   int block_head_base;           // block * heads: row of the cache's [blocks*heads] axis
   float scale_log2;              // softmax scale * log2(e)
   __nv_bfloat16* out;
   float* lse;                    // nullable
-  float* ws_o;                   // [splits][heads][nq][128] f32 (splits > 1)
-  float* ws_lse;                 // [splits][heads][nq]
+  float* ws_o;                   // [pieces][ctas per unit][256][128] f32 partial outputs (tail_splits > 1)
+  float* ws_lse;                 // [pieces][ctas per unit][256] partial log-sum-exps (natural log)
   const float* k_scale;          // int8 cache scales, [blocks*heads][scale_stride]
   const float* v_scale;
   long long scale_stride;        // cache slots per (block, head)
@@ -128,11 +141,19 @@ struct AttnParams {
   const int* sparse_counts;      // [heads][groups]
   int max_keep;
   int n_groups;                  // 512-query groups (two 256-query blocks each)
+  int block_heads;               // blocks * heads: planes of the cache (checked build)
+  long long ws_rows;             // partial-output rows the workspace holds (checked build)
 };
 
-cudaError_t launch_segment_attn(int kind, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
+// n_items = n_full + (units - n_full) * tail_splits work items.
+cudaError_t launch_segment_attn(int kind, const AttnTensorMaps& tm, const AttnParams& p, int n_items,
                                 cudaStream_t stream);
-cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
+// Merges the pieces of units n_full .. units-1 (tail_splits > 1 only).
+cudaError_t launch_attn_combine(const AttnParams& p, int units, int ctas_per_unit, cudaStream_t stream);
+// Work items of the attention kernel that run at once on the current device:
+// SMs for a BF16 cache (one CTA per SM), co-resident CTA pairs for one-byte
+// caches.  0 if the device cannot be queried.
+int attn_concurrent_items(int kind);
 int attn_smem_bytes(bool int8_cache);
 
 }  // namespace nomas

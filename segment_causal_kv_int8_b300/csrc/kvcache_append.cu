@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "rope_math.cuh"
 #include "sm100.cuh"
@@ -76,6 +77,7 @@ __device__ __forceinline__ void fp8_encode(const float (&x)[N], float inv, bool 
 template <int K>
 __device__ __forceinline__ void write_row(const AppendParams& p, int tensor, long long dst_row, const float (&x)[8],
                                           int g, unsigned gmask) {
+  if (!in_bounds(dst_row, 1, p.cache_rows, p.err)) return;  // uniform over the lane group
   if constexpr (K != kCacheBF16) {
     constexpr float kQMax = K == kCacheInt8 ? 127.0f : 448.0f;
     float m = 0.0f;
@@ -137,6 +139,7 @@ __device__ __forceinline__ void write_row(const AppendParams& p, int tensor, lon
 template <int K>
 __device__ __forceinline__ void store_row16(const AppendParams& p, int tensor, long long dst_row, const float (&x)[16],
                                             int g, unsigned gmask) {
+  if (!in_bounds(dst_row, 1, p.cache_rows, p.err)) return;  // uniform over the lane group
   if constexpr (K != kCacheBF16) {
     constexpr float kQMax = K == kCacheInt8 ? 127.0f : 448.0f;
     float m0 = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
@@ -226,7 +229,12 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
     const int n = n0 + r;
     if (n < p.n_tokens) {
       const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
-      load8<kF32In>(src, b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g, x[r]);
+      const long long off = b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g;
+      if (in_bounds(off, 8, p.src_extent, p.err))
+        load8<kF32In>(src, off, x[r]);
+      else
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[r][e] = 0.0f;
     }
   }
 #pragma unroll
@@ -263,9 +271,14 @@ __global__ void __launch_bounds__(256, K != kCacheBF16 ? 6 : 8) append8_kernel(c
     const int n = n0 + r;
     if (n < p.n_tokens) {
       const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
-      const uint4* q = reinterpret_cast<const uint4*>(src + b * p.block_stride + (src_tok * p.heads + h) * 128 + 16 * g);
-      w[r][0] = q[0];
-      w[r][1] = q[1];
+      const long long off = b * p.block_stride + (src_tok * p.heads + h) * 128 + 16 * g;
+      if (in_bounds(off, 16, p.src_extent, p.err)) {
+        const uint4* q = reinterpret_cast<const uint4*>(src + off);
+        w[r][0] = q[0];
+        w[r][1] = q[1];
+      } else {
+        w[r][0] = w[r][1] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 #pragma unroll
@@ -340,8 +353,13 @@ __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const 
         const char* src = static_cast<const char*>(tensor ? p.v : p.k) +
                           (b * p.block_stride + (static_cast<long long>(p.first_frame) * p.tpf + n0) * row_elems) * esz;
         const uint32_t bytes = static_cast<uint32_t>(nt * row_elems * esz);
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_load(stage_raw + s * kStageBytes, src, bytes, &full[s]);
+        if (in_bounds(b * p.block_stride + (static_cast<long long>(p.first_frame) * p.tpf + n0) * row_elems,
+                      nt * row_elems, p.src_extent, p.err)) {
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_load(stage_raw + s * kStageBytes, src, bytes, &full[s]);
+        } else {
+          mbar_arrive(&full[s]);  // nothing loaded; the slot's rows are written from stale data
+        }
       }
       if (!ok) {
         // Abort: give the loads already issued time to land.
@@ -432,7 +450,12 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant_
       const int n = n0 + r;
       if (n < p.n_tokens) {
         const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
-        load8<kF32In>(src, b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g, x[r]);
+        const long long off = b * p.block_stride + (src_tok * p.heads + h) * 128 + 8 * g;
+        if (in_bounds(off, 8, p.src_extent, p.err))
+          load8<kF32In>(src, off, x[r]);
+        else
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[r][e] = 0.0f;
       }
     }
   }
@@ -499,9 +522,15 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
   for (int r = 0; r < 2; ++r) {
     const long long row = r0 + (threadIdx.x >> 3) + 32 * r;
     if (row < rows) {
-      const uint4* q = reinterpret_cast<const uint4*>(src + row * 128 + 16 * g);
-      w[r][0] = q[0];
-      w[r][1] = q[1];
+      const long long off = b * p.block_stride + static_cast<long long>(p.first_frame) * p.tpf * p.heads * 128 +
+                            row * 128 + 16 * g;
+      if (in_bounds(off, 16, p.src_extent, p.err)) {
+        const uint4* q = reinterpret_cast<const uint4*>(src + row * 128 + 16 * g);
+        w[r][0] = q[0];
+        w[r][1] = q[1];
+      } else {
+        w[r][0] = w[r][1] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
   const int tok0 = static_cast<int>(r0 / p.heads);

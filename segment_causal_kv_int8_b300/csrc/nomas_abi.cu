@@ -132,52 +132,108 @@ nomas_status encode3d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64
   return r == CUDA_SUCCESS ? NOMAS_OK : NOMAS_ERR_CUDA;
 }
 
+// Work plan of one attention call (see AttnParams): units of one head x 256
+// query rows (BF16 cache) or x 512 rows in a CTA pair (one-byte caches);
+// units 0 .. n_full-1 run whole, every later unit in `splits` pieces of its
+// key-tile range.
 struct AttnPlan {
-  int nq, nc, n_pairs, n_cache_tiles, n_cur_tiles, splits;
+  int nq, nc, n_cache_tiles, n_cur_tiles;
+  int ctas;            // CTAs per unit
+  int units_per_head;
+  int units;
+  int n_full;
+  int splits;          // pieces per split unit (1 = nothing split)
+  int n_items;         // work items launched
   size_t ws_o_bytes, ws_lse_bytes;
 };
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-int auto_splits(int units, int n_tiles, int heads, int nq, int sms) {
-  // Modelled time in units of one CTA tile-iteration (256 queries x 128 keys,
-  // about 1.1 us): waves x (tiles per split + fixed cost) plus, for splits > 1,
-  // the combine pass (write + read of f32 partials) at ~6.5 TB/s.
-  double best = 1e300;
-  int best_s = 1;
-  const int s_max = std::min(8, std::max(1, n_tiles / 4));
-  for (int s = 1; s <= s_max; ++s) {
-    const double waves = std::ceil(static_cast<double>(units) * s / sms);
-    double cost = waves * (std::ceil(static_cast<double>(n_tiles) / s) + 1.5);
-    if (s > 1) {
-      const double bytes = (2.0 * s + 0.5) * heads * static_cast<double>(nq) * 128 * 4;
-      cost += bytes / 6.5e12 / 1.1e-6;
-    }
-    if (cost < best * 0.98) {
-      best = cost;
-      best_s = s;
-    }
-  }
-  return best_s;
+void plan_workspace(AttnPlan* pl) {
+  const size_t rows = pl->splits > 1 ? static_cast<size_t>(pl->units - pl->n_full) * pl->splits * pl->ctas * 256 : 0;
+  pl->ws_o_bytes = round256(rows * 128 * 4);
+  pl->ws_lse_bytes = round256(rows * 4);
+  pl->n_items = pl->n_full + (pl->units - pl->n_full) * pl->splits;
 }
 
-AttnPlan attn_plan(const nomas_kvcache* c, int32_t n_video, int32_t n_text, int32_t num_splits, int sms) {
+// Modelled time of a plan, in key-tile iterations of one CTA: waves of work
+// items on `slots` concurrent items, a fixed cost per item (Q load, pipeline
+// fill, epilogue), and for split units the combine pass (partials written by
+// the kernel and read back, about 6.5 TB/s, plus one launch).  Whole units
+// are dispatched first; the pieces fill the waves after them.
+double plan_cost(int units, int n_full, int splits, int n_tiles, int slots, int ctas, double tile_us) {
+  constexpr double kFixed = 2.5;
+  const int per_piece = (n_tiles + splits - 1) / splits;
+  double t = std::ceil(static_cast<double>(n_full) / slots) * (n_tiles + kFixed);
+  const int rest = units - n_full;
+  if (rest > 0) {
+    t += std::ceil(static_cast<double>(rest) * splits / slots) * (per_piece + kFixed);
+    if (splits > 1) {
+      const double bytes = static_cast<double>(rest) * ctas * 256 * (2.0 * splits * 516 + 256);
+      t += (bytes / 6.5e12 * 1e6 + 3.0) / tile_us;
+    }
+  }
+  return t;
+}
+
+// The plan nomas_segment_attn chooses for num_splits = 0: no split; or the
+// units of the last, partial wave each cut into s pieces (the whole units fill
+// the full waves); or every unit cut into s pieces.  Cheapest modelled time,
+// ties to fewer pieces.
+void auto_plan(AttnPlan* pl, int n_tiles, int slots, bool one_byte) {
+  const double tile_us = one_byte ? 2.0 : 1.6;
+  const int U = pl->units;
+  double best = plan_cost(U, U, 1, n_tiles, slots, pl->ctas, tile_us);
+  int best_full = U, best_s = 1;
+  const int s_max = std::min(8, std::max(1, n_tiles / 4));
+  const int tail_full = (U / slots) * slots;
+  for (int s = 2; s <= s_max; ++s) {
+    for (int full : {tail_full, 0}) {
+      if (full >= U) continue;
+      const double c = plan_cost(U, full, s, n_tiles, slots, pl->ctas, tile_us);
+      if (c < best * 0.98) {
+        best = c;
+        best_full = full;
+        best_s = s;
+      }
+    }
+  }
+  pl->n_full = best_full;
+  pl->splits = best_s;
+}
+
+// num_splits: 0 = automatic, 1 = no split, s > 1 = every unit in s pieces.
+// n_tiles_eff (> 0) replaces the dense key-tile count in the automatic choice
+// (block-sparse attention).
+AttnPlan attn_plan(const nomas_kvcache* c, int32_t n_video, int32_t n_text, int32_t num_splits, int slots,
+                   int n_tiles_eff = 0) {
   AttnPlan pl;
   pl.nq = n_video + n_text;
   pl.nc = static_cast<int>(static_cast<int64_t>(c->valid_frames) * c->grid_h * c->grid_w);
-  pl.n_pairs = (pl.nq + 255) / 256;
   pl.n_cache_tiles = (pl.nc + 127) / 128;
   pl.n_cur_tiles = (pl.nq + 127) / 128;
+  const bool one_byte = quantised(c);
+  pl.ctas = one_byte ? 2 : 1;
+  const int n_qblocks = (pl.nq + 255) / 256;
+  pl.units_per_head = one_byte ? (n_qblocks + 1) / 2 : n_qblocks;
+  pl.units = pl.units_per_head * c->heads;
   const int n_tiles = pl.n_cache_tiles + pl.n_cur_tiles;
-  int s = num_splits;
-  if (s <= 0) s = auto_splits(pl.n_pairs * c->heads, n_tiles, c->heads, pl.nq, sms > 0 ? sms : 148);
-  s = std::max(1, std::min(s, std::min(n_tiles, 64)));
-  pl.splits = s;
-  pl.ws_o_bytes = s > 1 ? round256(static_cast<size_t>(s) * c->heads * pl.nq * 128 * 4) : 0;
-  pl.ws_lse_bytes = s > 1 ? round256(static_cast<size_t>(s) * c->heads * pl.nq * 4) : 0;
+  if (num_splits == 0) {
+    auto_plan(&pl, n_tiles_eff > 0 ? n_tiles_eff : n_tiles,
+              slots > 0 ? slots : (one_byte ? 74 : 148), one_byte);
+  } else {
+    const int s = std::max(1, std::min(num_splits, std::min(n_tiles, 64)));
+    pl.splits = s;
+    pl.n_full = s > 1 ? 0 : pl.units;
+  }
+  plan_workspace(&pl);
   return pl;
 }
 
+// Concurrent work items of the attention kernel on the current device.
+int attn_slots(const nomas_kvcache* c) {
+  return attn_concurrent_items(cache_kind(c));
+}
 }  // namespace
 }  // namespace nomas
 
@@ -265,6 +321,9 @@ NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, i
   p.tpf = grid_h * grid_w;
   p.grid_w = grid_w;
   p.t0 = t0;
+  p.extent = (static_cast<long long>(n_video) - 1) * row_stride_elems + static_cast<long long>(heads) * head_dim;
+  p.err = nullptr;
+  if (device_state(&p.err, nullptr) != NOMAS_OK) p.err = nullptr;
   return from_cuda(launch_rope3d(io_dt == NOMAS_BF16, q, k, p, stream));
 }
 
@@ -310,6 +369,8 @@ nomas_status append_impl(nomas_kvcache* cache, const void* k, const void* v, nom
     p.vs = cache->v_scale;
     p.chunk_tokens = 0;
     p.err = nullptr;
+    p.src_extent = static_cast<long long>(cache->num_blocks - 1) * block_stride_elems + seg_elems;
+    p.cache_rows = static_cast<long long>(cache->num_blocks) * cache->heads * p.cap_slots;
     int sms = 0;
     if (device_state(&p.err, &sms) != NOMAS_OK) {
       p.err = nullptr;
@@ -461,29 +522,55 @@ NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory
   return NOMAS_OK;
 }
 
-NOMAS_API nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
-                                                          int32_t num_splits, size_t* bytes) {
+namespace {
+// The plan a call with these arguments runs (host only; the automatic choice
+// depends on the current device's SM count).
+nomas_status query_plan(const nomas_kvcache* cache, int32_t n_video, int32_t n_text, int32_t num_splits,
+                        AttnPlan* pl) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
-  if (bytes == nullptr || n_video < 0 || n_text < 0 || num_splits < 0) return NOMAS_ERR_INVALID_ARG;
-  int sms = 148;
-  if (num_splits == 0) {
-    // The automatic split count depends on the device's SM count.
-    if (device_state(nullptr, &sms) != NOMAS_OK) sms = 148;
-  }
-  const AttnPlan pl = attn_plan(cache, n_video, n_text, num_splits, sms);
+  if (n_video < 0 || n_text < 0 || num_splits < 0) return NOMAS_ERR_INVALID_ARG;
+  *pl = attn_plan(cache, n_video, n_text, num_splits, num_splits == 0 ? attn_slots(cache) : 0);
+  return NOMAS_OK;
+}
+}  // namespace
+
+NOMAS_API nomas_status nomas_segment_attn_workspace_bytes(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
+                                                          int32_t num_splits, size_t* bytes) {
+  if (bytes == nullptr) return NOMAS_ERR_INVALID_ARG;
+  AttnPlan pl;
+  const nomas_status st = query_plan(cache, n_video, n_text, num_splits, &pl);
+  if (st != NOMAS_OK) return st;
   *bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
+  return NOMAS_OK;
+}
+
+NOMAS_API nomas_status nomas_segment_attn_plan(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
+                                               int32_t num_splits, nomas_attn_plan* out) {
+  if (out == nullptr) return NOMAS_ERR_INVALID_ARG;
+  AttnPlan pl;
+  const nomas_status st = query_plan(cache, n_video, n_text, num_splits, &pl);
+  if (st != NOMAS_OK) return st;
+  out->units = pl.units;
+  out->whole_units = pl.n_full;
+  out->pieces_per_split_unit = pl.splits;
+  out->ctas_per_unit = pl.ctas;
+  out->work_items = pl.n_items;
+  out->reserved = 0;
+  out->workspace_bytes = pl.ws_o_bytes + pl.ws_lse_bytes;
   return NOMAS_OK;
 }
 
 namespace {
 // Dense attention (tiles == nullptr) or block-sparse attention over kept
-// cache-tile lists.  The split plan is the dense one either way, so both need
-// the workspace nomas_segment_attn_workspace_bytes reports.
+// cache-tile lists.  The workspace nomas_segment_attn_workspace_bytes reports
+// for the same num_splits suffices for both.  `forced` (nullable) replaces
+// the plan num_splits would give.
 nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const void* q, const void* k_cur,
                                const void* v_cur, int32_t n_video, int32_t n_text, float softmax_scale, void* out,
                                float* lse, void* workspace, size_t workspace_bytes, int32_t num_splits,
-                               const int32_t* tiles, const int32_t* counts, int32_t max_keep, cudaStream_t stream) {
+                               const int32_t* tiles, const int32_t* counts, int32_t max_keep,
+                               const AttnPlan* forced, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;
   if (block < 0 || block >= cache->num_blocks || n_video < 0 || n_text < 0 || num_splits < 0)
@@ -497,23 +584,24 @@ nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const 
   if (nq64 == 0) return NOMAS_OK;
   if (nq64 > (int64_t(1) << 28)) return NOMAS_ERR_UNSUPPORTED;
   uint32_t* err = nullptr;
-  int sms = 0;
-  st = device_state(&err, &sms);
+  st = device_state(&err, nullptr);
   if (st != NOMAS_OK) return st;
-  AttnPlan pl = attn_plan(cache, n_video, n_text, num_splits, sms);
-  if (tiles != nullptr && num_splits == 0 && pl.splits > 1) {
-    // Block-sparse: plan for at most max_keep cache tiles per CTA, never more
-    // splits than the dense plan (whose workspace the caller sized).
+  const int slots = num_splits == 0 ? attn_slots(cache) : 0;
+  AttnPlan pl = forced ? *forced : attn_plan(cache, n_video, n_text, num_splits, slots);
+  if (!forced && tiles != nullptr && num_splits == 0) {
+    // Block-sparse: plan for at most max_keep cache tiles per unit; keep the
+    // dense plan (whose workspace the caller sized) if the sparse one needs more.
+    const AttnPlan dense = pl;
     const int eff = std::min(max_keep, pl.n_cache_tiles) + pl.n_cur_tiles;
-    const int s = std::max(1, std::min(auto_splits(pl.n_pairs * cache->heads, eff, cache->heads, pl.nq,
-                                                   sms > 0 ? sms : 148), eff));
-    if (s < pl.splits) pl = attn_plan(cache, n_video, n_text, s, sms);
+    pl = attn_plan(cache, n_video, n_text, 0, slots, std::max(1, eff));
+    if (pl.ws_o_bytes + pl.ws_lse_bytes > dense.ws_o_bytes + dense.ws_lse_bytes) pl = dense;
   }
   if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_o_bytes + pl.ws_lse_bytes ||
                         (reinterpret_cast<uintptr_t>(workspace) & 255u))) {
-    if (num_splits > 1) return NOMAS_ERR_INVALID_ARG;  // an explicit split count needs its workspace
-    pl = attn_plan(cache, n_video, n_text, 1, sms);
+    if (num_splits > 1 || forced) return NOMAS_ERR_INVALID_ARG;  // an explicit split count needs its workspace
+    pl = attn_plan(cache, n_video, n_text, 1, 0);
   }
+  if (pl.n_items <= 0 || static_cast<int64_t>(pl.n_items) * pl.ctas > 0x7FFFFFFF) return NOMAS_ERR_UNSUPPORTED;
   const bool int8 = quantised(cache);  // one-byte codes (INT8 or FP8): staged and dequantised in the kernel
   AttnTensorMaps tm;
   memset(&tm, 0, sizeof(tm));
@@ -552,7 +640,9 @@ nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const 
   p.heads = cache->heads;
   p.n_cache_tiles = pl.n_cache_tiles;
   p.n_cur_tiles = pl.n_cur_tiles;
-  p.num_splits = pl.splits;
+  p.units_per_head = pl.units_per_head;
+  p.n_full = pl.n_full;
+  p.tail_splits = pl.splits;
   p.block_head_base = block * cache->heads;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -567,8 +657,10 @@ nomas_status segment_attn_impl(const nomas_kvcache* cache, int32_t block, const 
   p.sparse_counts = counts;
   p.max_keep = max_keep;
   p.n_groups = (pl.nq + 511) / 512;
-  st = from_cuda(launch_segment_attn(cache_kind(cache), tm, p, pl.n_pairs, stream));
-  if (st == NOMAS_OK && pl.splits > 1) st = from_cuda(launch_attn_combine(p, stream));
+  p.block_heads = cache->num_blocks * cache->heads;
+  p.ws_rows = pl.splits > 1 ? static_cast<long long>(pl.units - pl.n_full) * pl.splits * pl.ctas * 256 : 0;
+  st = from_cuda(launch_segment_attn(cache_kind(cache), tm, p, pl.n_items, stream));
+  if (st == NOMAS_OK && pl.splits > 1) st = from_cuda(launch_attn_combine(p, pl.units, pl.ctas, stream));
   return st;
 }
 
@@ -583,7 +675,29 @@ NOMAS_API nomas_status nomas_segment_attn(const nomas_kvcache* cache, int32_t bl
                                           void* out, float* lse, void* workspace, size_t workspace_bytes,
                                           int32_t num_splits, cudaStream_t stream) {
   return segment_attn_impl(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, workspace,
-                           workspace_bytes, num_splits, nullptr, nullptr, 0, stream);
+                           workspace_bytes, num_splits, nullptr, nullptr, 0, nullptr, stream);
+}
+
+NOMAS_API nomas_status nomas_segment_attn_planned(const nomas_kvcache* cache, int32_t block, const void* q,
+                                                  const void* k_cur, const void* v_cur, int32_t n_video,
+                                                  int32_t n_text, float softmax_scale, void* out, float* lse,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  const nomas_attn_plan* plan, cudaStream_t stream) {
+  if (plan == nullptr) return NOMAS_ERR_INVALID_ARG;
+  AttnPlan pl;
+  nomas_status st = query_plan(cache, n_video, n_text, 1, &pl);
+  if (st != NOMAS_OK) return st;
+  const int n_tiles = pl.n_cache_tiles + pl.n_cur_tiles;
+  if (plan->units != pl.units || plan->ctas_per_unit != pl.ctas || plan->whole_units < 0 ||
+      plan->whole_units > pl.units || plan->pieces_per_split_unit < 1 ||
+      plan->pieces_per_split_unit > std::max(1, std::min(n_tiles, 64)))
+    return NOMAS_ERR_INVALID_ARG;
+  pl.n_full = plan->whole_units;
+  pl.splits = plan->whole_units == pl.units ? 1 : plan->pieces_per_split_unit;
+  if (pl.splits == 1) pl.n_full = pl.units;
+  plan_workspace(&pl);
+  return segment_attn_impl(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, workspace,
+                           workspace_bytes, 0, nullptr, nullptr, 0, &pl, stream);
 }
 
 NOMAS_API nomas_status nomas_sparse_select_workspace_bytes(const nomas_kvcache* cache, int32_t n_video, int32_t n_text,
@@ -650,7 +764,7 @@ NOMAS_API nomas_status nomas_segment_attn_sparse(const nomas_kvcache* cache, int
   if ((reinterpret_cast<uintptr_t>(tiles) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u))
     return NOMAS_ERR_INVALID_ARG;
   return segment_attn_impl(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, workspace,
-                           workspace_bytes, num_splits, tiles, counts, max_keep, stream);
+                           workspace_bytes, num_splits, tiles, counts, max_keep, nullptr, stream);
 }
 
 NOMAS_API nomas_status nomas_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
@@ -723,15 +837,27 @@ NOMAS_API nomas_status nomas_segment_attn_noalloc(const nomas_kvcache* cache, in
                                                   const void* k_cur, const void* v_cur, int32_t n_video,
                                                   int32_t n_text, float softmax_scale, void* out, float* lse,
                                                   int32_t num_splits, cudaStream_t stream) {
-  size_t need = 0;
-  nomas_status st = nomas_segment_attn_workspace_bytes(cache, n_video, n_text, num_splits, &need);
+  AttnPlan pl;
+  nomas_status st = query_plan(cache, n_video, n_text, num_splits, &pl);
   if (st != NOMAS_OK) return st;
-  if (need > static_cast<size_t>(NOMAS_NOALLOC_SCRATCH_BYTES)) return NOMAS_ERR_CAPACITY;
+  constexpr size_t kCap = static_cast<size_t>(NOMAS_NOALLOC_SCRATCH_BYTES);
+  if (pl.ws_o_bytes + pl.ws_lse_bytes > kCap) {
+    // An explicit piece count that does not fit is refused.  The automatic
+    // plan instead keeps its whole units and cuts the rest into fewer pieces,
+    // down to none, until the scratch fits.
+    if (num_splits != 0) return NOMAS_ERR_CAPACITY;
+    while (pl.splits > 1 && pl.ws_o_bytes + pl.ws_lse_bytes > kCap) {
+      --pl.splits;
+      if (pl.splits == 1) pl.n_full = pl.units;
+      plan_workspace(&pl);
+    }
+  }
+  const size_t need = pl.ws_o_bytes + pl.ws_lse_bytes;
   void* scratch = nullptr;
   if (need > 0) {
     st = noalloc_scratch(&scratch);
     if (st != NOMAS_OK) return st;
   }
-  return nomas_segment_attn(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, scratch,
-                            need, num_splits, stream);
+  return segment_attn_impl(cache, block, q, k_cur, v_cur, n_video, n_text, softmax_scale, out, lse, scratch, need,
+                           num_splits, nullptr, nullptr, 0, &pl, stream);
 }

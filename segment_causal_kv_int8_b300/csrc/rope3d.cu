@@ -5,17 +5,22 @@
 // into contiguous chunks per axis; pair (x[o+2i], x[o+2i+1]) of the chunk of
 // axis a rotates by pos_a * f_{a,i}, f_{a,i} = theta^(-2i/d_a).
 //
-// HBM-bound elementwise kernel: 16 threads own one token, each thread four
-// consecutive pairs (one 16-byte bf16 vector or two float4 of a head row) of a
-// group of heads.  The cos/sin of a (token, pair) is computed once per head
-// group and applied to those heads of Q and K (angle arithmetic in
-// rope_math.cuh).
+// HBM-bound elementwise kernel.  Each CTA takes a contiguous run of tokens:
+// it first computes the cos/sin of every (token, pair) of the run once into
+// shared memory (angle arithmetic in rope_math.cuh), then streams the rows of
+// Q and K as 16-byte vectors, one vector per thread per tensor and token, two
+// tokens in flight per thread.  The grid is one resident wave of CTAs with
+// equal token runs, so no partial last wave.  A thread's vectors always hold
+// the same rotary pairs, so its table reads are two consecutive 16-byte
+// loads.  The cos/sin of a pair depend only on its position and frequency, so
+// the rotation is bit for bit what per-element evaluation gives.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <type_traits>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "rope_math.cuh"
 
@@ -47,6 +52,8 @@ __global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void*
 #pragma unroll
   for (int e = 0; e < 4; ++e) any |= p.axis[4 * g + e] >= 0;
   if (!any) return;
+  if (!in_bounds(static_cast<long long>(tok) * p.row_stride + h0 * 128 + 8 * g, (nh - 1) * 128 + 8, p.extent, p.err))
+    return;
   const int nt = (k != nullptr) ? 2 : 1;
   using Vec = typename std::conditional<kBF16, uint4, float4>::type;
   constexpr int kVecs = kBF16 ? 1 : 2;  // 16-byte vectors per 8-value group
@@ -118,14 +125,150 @@ __global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void*
   }
 }
 
+constexpr int kRunMax = 32;  // tokens of one table fill (32 x 64 pairs x 8 B = 16 KB of shared memory)
+
+// Streams the video rows of Q and K (row_stride elements apart) as 16-byte
+// vectors: V = heads * VPR vectors per token, VPR = 16 (bf16) or 32 (f32).
+template <bool kBF16>
+__global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, void* __restrict__ k,
+                                                         const __grid_constant__ RopeParams p, TwoPi tp,
+                                                         int run_tokens) {
+  constexpr int VPR = kBF16 ? 16 : 32;  // vectors per head row
+  constexpr int PPV = kBF16 ? 4 : 2;    // rotary pairs per vector
+  constexpr int ESZ = kBF16 ? 2 : 4;
+  using Vec = typename std::conditional<kBF16, uint4, float4>::type;
+  __shared__ __align__(16) float2 cs[kRunMax * 64];   // (cos, sin) of [token of the fill][pair]
+  __shared__ int8_t axis_s[64];
+  const int tid = threadIdx.x;
+  if (tid < 64) axis_s[tid] = p.axis[tid];
+  const int tok_begin = blockIdx.x * run_tokens;
+  const int tok_end = min(p.n_video, tok_begin + run_tokens);
+  const int V = p.heads * VPR;
+  // Fixed per thread: which tokens of a fill (t_off, t_off + tpi, ...) and
+  // which vectors of a token row (rem, rem + 256, ...) it handles.
+  const int tpi = V >= 256 ? 1 : 256 / V;   // tokens per pass of the CTA
+  const int t_off = V >= 256 ? 0 : tid / V;
+  const int rem0 = V >= 256 ? tid : tid - t_off * V;
+  const bool active = t_off < tpi;
+  const int g = rem0 & (VPR - 1);           // the thread's pair group
+  __syncthreads();
+  bool rotated = false;
+#pragma unroll
+  for (int e = 0; e < PPV; ++e) rotated |= axis_s[g * PPV + e] >= 0;
+  const int nt = (k != nullptr) ? 2 : 1;
+  for (int f0 = tok_begin; f0 < tok_end; f0 += kRunMax) {
+    const int nf = min(kRunMax, tok_end - f0);
+    // cos/sin of the fill's tokens: entry (t, pair) at t * 64 + pair
+    for (int e = tid; e < nf * 64; e += 256) {
+      const int t = e >> 6, pair = e & 63;
+      const int a = axis_s[pair];
+      float c = 1.0f, sn = 0.0f;
+      if (a >= 0) {
+        const int tok = f0 + t;
+        const int frame = tok / p.tpf;
+        const int within = tok - frame * p.tpf;
+        const int row = within / p.grid_w;
+        const float pos = a == 0 ? static_cast<float>(p.t0 + frame)
+                                 : static_cast<float>(a == 1 ? row : within - row * p.grid_w);
+        sincosf(rope_reduced_angle(pos, p.f_hi[pair], p.f_lo[pair], tp), &sn, &c);
+      }
+      cs[e] = make_float2(c, sn);
+    }
+    __syncthreads();
+    if (active && rotated) {
+      for (int tl = t_off; tl < nf; tl += 2 * tpi) {
+        const int tl1 = tl + tpi;
+        const bool two = tl1 < nf;
+        for (int rem = rem0; rem < V; rem += 256) {
+          const int head = rem / VPR;
+          // element offset of this vector in token f0 + tl (and f0 + tl1)
+          const long long off0 = static_cast<long long>(f0 + tl) * p.row_stride + head * 128 + g * (16 / ESZ);
+          const long long off1 = off0 + static_cast<long long>(tpi) * p.row_stride;
+          if (!in_bounds(off0, 16 / ESZ, p.extent, p.err) || (two && !in_bounds(off1, 16 / ESZ, p.extent, p.err)))
+            continue;
+          Vec w[2][2];
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            if (which >= nt) break;
+            const Vec* base = reinterpret_cast<const Vec*>(static_cast<const char*>(which ? k : q));
+            w[which][0] = base[off0 * ESZ / 16];
+            if (two) w[which][1] = base[off1 * ESZ / 16];
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u == 1 && !two) break;
+            const float4* tab = reinterpret_cast<const float4*>(&cs[(tl + u * tpi) * 64 + g * PPV]);
+            float cc[PPV], ss[PPV];
+#pragma unroll
+            for (int h2 = 0; h2 < PPV / 2; ++h2) {
+              const float4 t4 = tab[h2];
+              cc[2 * h2] = t4.x;
+              ss[2 * h2] = t4.y;
+              cc[2 * h2 + 1] = t4.z;
+              ss[2 * h2 + 1] = t4.w;
+            }
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+              if (which >= nt) break;
+              Vec o;
+              if constexpr (kBF16) {
+                const uint32_t* v = reinterpret_cast<const uint32_t*>(&w[which][u]);
+                uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float x0 = __uint_as_float(v[e] << 16);
+                  float x1 = __uint_as_float(v[e] & 0xFFFF0000u);
+                  rope_rotate_pair(x0, x1, cc[e], ss[e]);
+                  __nv_bfloat162 t2 = __floats2bfloat162_rn(x0, x1);
+                  ov[e] = *reinterpret_cast<const uint32_t*>(&t2);
+                }
+              } else {
+                const float* v = reinterpret_cast<const float*>(&w[which][u]);
+                float x[4] = {v[0], v[1], v[2], v[3]};
+                rope_rotate_pair(x[0], x[1], cc[0], ss[0]);
+                rope_rotate_pair(x[2], x[3], cc[1], ss[1]);
+                o = make_float4(x[0], x[1], x[2], x[3]);
+              }
+              Vec* base = reinterpret_cast<Vec*>(static_cast<char*>(which ? k : q));
+              base[(u ? off1 : off0) * ESZ / 16] = o;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream) {
   if (p.n_video <= 0) return cudaSuccess;
+  const TwoPi tp = rope_two_pi();
+  // One resident wave of CTAs with equal token runs.
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+    const cudaError_t e = bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<true>, 256, 0)
+                                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<false>, 256, 0);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      per_sm = 0;
+    }
+  }
+  if (per_sm > 0) {
+    const long long slots = static_cast<long long>(sms) * per_sm;
+    const int run = static_cast<int>((p.n_video + slots - 1) / slots);
+    const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);
+    if (bf16_io)
+      rope3d_run_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp, run);
+    else
+      rope3d_run_kernel<false><<<grid, 256, 0, stream>>>(q, k, p, tp, run);
+    return cudaGetLastError();
+  }
   const dim3 grid(static_cast<unsigned>((p.n_video + 15) / 16),
                   static_cast<unsigned>((p.heads + kRopeHeadsPerThread - 1) / kRopeHeadsPerThread));
   if (grid.y > 65535) return cudaErrorInvalidValue;
-  const TwoPi tp = rope_two_pi();
   if (bf16_io)
     rope3d_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp);
   else

@@ -35,6 +35,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
 
@@ -97,14 +98,14 @@ struct KeyTiles {
   const int* list;  // null: cache tiles 0 .. n_cache-1
 };
 
-__device__ __forceinline__ KeyTiles key_tiles(const AttnParams& p, int head) {
+__device__ __forceinline__ KeyTiles key_tiles(const AttnParams& p, int head, int qblk) {
   KeyTiles kt;
   if (p.sparse_tiles == nullptr) {
     kt.n_cache = p.n_cache_tiles;
     kt.list = nullptr;
   } else {
     // Query group = two consecutive 256-query blocks (one CTA pair for INT8).
-    const size_t hg = static_cast<size_t>(head) * p.n_groups + (blockIdx.x >> 1);
+    const size_t hg = static_cast<size_t>(head) * p.n_groups + (qblk >> 1);
     kt.n_cache = min(max(p.sparse_counts[hg], 0), min(p.max_keep, p.n_cache_tiles));
     kt.list = p.sparse_tiles + hg * p.max_keep;
   }
@@ -131,11 +132,6 @@ __device__ __forceinline__ TileInfo tile_info(int j, const AttnParams& p, const 
   return t;
 }
 
-// int8 code byte -> float via the 2^23 magic number: (2^23 + (c + 128)) - (2^23 + 128) = c.
-__device__ __forceinline__ float i8_to_f32(uint32_t biased, uint32_t sel) {
-  return __uint_as_float(__byte_perm(biased, 0x4B000000u, sel)) - 8388736.0f;
-}
-
 template <bool kInt8, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     segment_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kcur,
@@ -150,13 +146,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int head = blockIdx.y;
-  const int split = blockIdx.z;
-  const int q_row0 = blockIdx.x * 256;
-  const KeyTiles kt = key_tiles(p, head);
+  // Work item -> (unit, piece).  One-byte caches launch clusters of two CTAs
+  // along x, both on the same item; CTA r of the pair takes query block
+  // 2 * (unit's block pair) + r.
+  const int item = kInt8 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int pair_rank = kInt8 ? static_cast<int>(blockIdx.x & 1u) : 0;
+  int unit, split, nsplit;
+  if (item < p.n_full) {
+    unit = item;
+    split = 0;
+    nsplit = 1;
+  } else {
+    const int j = item - p.n_full;
+    unit = p.n_full + j / p.tail_splits;
+    split = j - (j / p.tail_splits) * p.tail_splits;
+    nsplit = p.tail_splits;
+  }
+  const int head = unit / p.units_per_head;
+  const int ublk = unit - head * p.units_per_head;
+  const int qblk = kInt8 ? 2 * ublk + pair_rank : ublk;
+  const int q_row0 = qblk * 256;
+  // Partial-output slot of a piece: [pieces][ctas per unit][256 rows].
+  const size_t piece_row0 =
+      nsplit > 1 ? (static_cast<size_t>(item - p.n_full) * (kInt8 ? 2 : 1) + static_cast<size_t>(pair_rank)) * 256
+                 : 0;
+  const KeyTiles kt = key_tiles(p, head, qblk);
   const int n_tiles = kt.n_cache + p.n_cur_tiles;
-  const int t_begin = static_cast<int>((static_cast<long long>(split) * n_tiles) / p.num_splits);
-  const int t_end = static_cast<int>((static_cast<long long>(split + 1) * n_tiles) / p.num_splits);
+  const int t_begin = static_cast<int>((static_cast<long long>(split) * n_tiles) / nsplit);
+  const int t_end = static_cast<int>((static_cast<long long>(split + 1) * n_tiles) / nsplit);
   const int n_iter = t_end - t_begin;
   const int bh = p.block_head_base + head;
 
@@ -238,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             uint64_t* fb = &bars[L::bStageFull + si];
+            (void)(in_bounds(ti.row0, 1, p.nc, p.err) && in_bounds(bh, 1, p.block_heads, p.err));
             mbar_arrive_expect_tx(fb, kI8HalfBytes);
             tma_load_3d(sStage + si * kI8HalfBytes, kv ? &tm_vc : &tm_kc, fb, 0, ti.row0 + 64 * static_cast<int>(rank),
                         bh);
@@ -251,6 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             uint64_t* fb = &bars[L::bRingFull + s];
+            (void)(ti.cache ? in_bounds(ti.row0, 1, p.nc, p.err) && in_bounds(bh, 1, p.block_heads, p.err)
+                            : in_bounds(ti.row0, 1, p.nq, p.err));
             mbar_arrive_expect_tx(fb, kTileBytes);
             uint8_t* dst = sRing + s * kTileBytes;
             for (int pn = 0; pn < 2; ++pn) {
@@ -485,12 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_iter > 0 && warp_wait(&bars[L::bPVDone + t], 0, ab, p.err)) {
       tc_fence_after();
       const int grow = q_row0 + t * 128 + row;
-      const bool live = grow < p.nq;
+      bool live = grow < p.nq;
       const float inv_l = 1.0f / l;
       const float lse_val = (m + log2f(l)) * kLn2;
       uint32_t v[32];
-      if (p.num_splits == 1) {
+      if (nsplit == 1) {
         __nv_bfloat16* dst = p.out + (static_cast<size_t>(grow) * p.heads + head) * 128;
+        live = live && in_bounds((static_cast<long long>(grow) * p.heads + head) * 128, 128,
+                                 static_cast<long long>(p.nq) * p.heads * 128, p.err);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           tmem_ld_x32(lane_base + o_col + 32 * c, v);
@@ -508,7 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (live && p.lse) p.lse[static_cast<size_t>(head) * p.nq + grow] = lse_val;
       } else {
-        float* dst = p.ws_o + ((static_cast<size_t>(split) * p.heads + head) * p.nq + grow) * 128;
+        const size_t prow = piece_row0 + t * 128 + row;
+        float* dst = p.ws_o + prow * 128;
+        live = live && in_bounds(static_cast<long long>(prow), 1, p.ws_rows, p.err);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           tmem_ld_x32(lane_base + o_col + 32 * c, v);
@@ -521,17 +545,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (live) p.ws_lse[(static_cast<size_t>(split) * p.heads + head) * p.nq + grow] = lse_val;
+        if (live) p.ws_lse[prow] = lse_val;
       }
-    } else if (ok && n_iter == 0 && p.num_splits > 1) {
-      // A split with no key tile (a block-sparse list shorter than the split
+    } else if (ok && n_iter == 0 && nsplit > 1) {
+      // A piece with no key tile (a block-sparse list shorter than the piece
       // count) contributes weight zero to the combine: O = 0, LSE = -inf.
       const int grow = q_row0 + t * 128 + row;
-      if (grow < p.nq) {
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + ((static_cast<size_t>(split) * p.heads + head) * p.nq + grow) * 128);
+      if (grow < p.nq && in_bounds(static_cast<long long>(piece_row0 + t * 128 + row), 1, p.ws_rows, p.err)) {
+        const size_t prow = piece_row0 + t * 128 + row;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * 128);
 #pragma unroll 4
         for (int c = 0; c < 32; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.ws_lse[(static_cast<size_t>(split) * p.heads + head) * p.nq + grow] = -INFINITY;
+        p.ws_lse[prow] = -INFINITY;
       }
     }
   } else if (warp >= 12) {
@@ -580,8 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int si = ri % L::NI, ui = ri / L::NI;
           const float* sp = kv ? p.v_scale : p.k_scale;
-          const float sc =
-              (trow < ti.valid) ? sp[static_cast<size_t>(bh) * p.scale_stride + ti.row0 + trow] : 0.0f;
+          const long long sidx = static_cast<long long>(bh) * p.scale_stride + ti.row0 + trow;
+          const float sc = (trow < ti.valid && in_bounds(sidx, 1, static_cast<long long>(p.block_heads) * p.scale_stride,
+                                                          p.err))
+                               ? sp[sidx]
+                               : 0.0f;
           if (!warp_wait(&bars[L::bStageFull + si], ui & 1, ab, p.err)) {
             ok = false;
             break;
@@ -612,13 +640,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[2 * e + 1] = pack_bf16x2(b.x * sc, b.y * sc);
               }
             } else {
+              // int8 code byte -> float via the 2^23 magic number: the biased
+              // byte c + 128 in the low mantissa bits of 2^23 gives the float
+              // 2^23 + 128 + c, and subtracting 2^23 + 128 leaves c exactly;
+              // then one rounded multiply by the row scale.  Packed f32x2 pairs.
               const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+              const uint64_t bias2 = f2_pack(-8388736.0f, -8388736.0f);
+              const uint64_t sc2 = f2_pack(sc, sc);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float f0 = i8_to_f32(wd[e], 0x7540u) * sc;
-                const float f1 = i8_to_f32(wd[e], 0x7541u) * sc;
-                const float f2 = i8_to_f32(wd[e], 0x7542u) * sc;
-                const float f3 = i8_to_f32(wd[e], 0x7543u) * sc;
+                const uint64_t c01 = f2_add(f2_pack(__uint_as_float(__byte_perm(wd[e], 0x4B000000u, 0x7540u)),
+                                                    __uint_as_float(__byte_perm(wd[e], 0x4B000000u, 0x7541u))),
+                                            bias2);
+                const uint64_t c23 = f2_add(f2_pack(__uint_as_float(__byte_perm(wd[e], 0x4B000000u, 0x7542u)),
+                                                    __uint_as_float(__byte_perm(wd[e], 0x4B000000u, 0x7543u))),
+                                            bias2);
+                float f0, f1, f2, f3;
+                f2_unpack(f2_mul(c01, sc2), f0, f1);
+                f2_unpack(f2_mul(c23, sc2), f2, f3);
                 o[2 * e] = pack_bf16x2(f0, f1);
                 o[2 * e + 1] = pack_bf16x2(f2, f3);
               }
@@ -686,24 +725,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine per-split partial outputs in split order: O = sum_s w_s O_s / sum_s w_s,
-// w_s = exp(lse_s - max lse), LSE = max + log(sum w_s).  One warp per (head, row).
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
-                                                      int splits, int heads, int nq, __nv_bfloat16* __restrict__ out,
-                                                      float* __restrict__ lse) {
+// Combine the pieces of every split unit in piece order: O = sum_s w_s O_s /
+// sum_s w_s, w_s = exp(lse_s - max lse), LSE = max + log(sum w_s).  One warp
+// per (split unit, CTA of the unit, query row).
+__global__ void __launch_bounds__(256) combine_kernel(const AttnParams p, int n_split_units, int ctas) {
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (gw >= static_cast<long long>(heads) * nq) return;
-  const int h = static_cast<int>(gw / nq);
-  const int r = static_cast<int>(gw % nq);
+  if (gw >= static_cast<long long>(n_split_units) * ctas * 256) return;
+  const int r = static_cast<int>(gw & 255);
+  const int c = static_cast<int>((gw >> 8) % ctas);
+  const int su = static_cast<int>((gw >> 8) / ctas);
+  const int unit = p.n_full + su;
+  const int head = unit / p.units_per_head;
+  const int ublk = unit - head * p.units_per_head;
+  const int grow = (ctas == 2 ? 2 * ublk + c : ublk) * 256 + r;
+  if (grow >= p.nq) return;
+  const int S = p.tail_splits;
+  auto prow = [&](int s) { return ((static_cast<size_t>(su) * S + s) * ctas + c) * 256 + r; };
+  if (!in_bounds(static_cast<long long>(prow(S - 1)), 1, p.ws_rows, p.err) ||
+      !in_bounds((static_cast<long long>(grow) * p.heads + head) * 128, 128, static_cast<long long>(p.nq) * p.heads * 128,
+                 p.err))
+    return;
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ws_lse[(static_cast<size_t>(s) * heads + h) * nq + r]);
+  for (int s = 0; s < S; ++s) mx = fmaxf(mx, p.ws_lse[prow(s)]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.0f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t row = (static_cast<size_t>(s) * heads + h) * nq + r;
-    const float w = expf(ws_lse[row] - mx);
-    const float4 o = *reinterpret_cast<const float4*>(ws_o + row * 128 + 4 * lane);
+  for (int s = 0; s < S; ++s) {
+    const size_t row = prow(s);
+    const float w = expf(p.ws_lse[row] - mx);
+    const float4 o = *reinterpret_cast<const float4*>(p.ws_o + row * 128 + 4 * lane);
     acc.x += w * o.x;
     acc.y += w * o.y;
     acc.z += w * o.z;
@@ -714,29 +764,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   uint2 pk;
   pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(out + (static_cast<size_t>(r) * heads + h) * 128 + 4 * lane) = pk;
-  if (lse && lane == 0) lse[static_cast<size_t>(h) * nq + r] = mx + logf(wsum);
+  *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(grow) * p.heads + head) * 128 + 4 * lane) = pk;
+  if (p.lse && lane == 0) p.lse[static_cast<size_t>(head) * p.nq + grow] = mx + logf(wsum);
 }
 
 template <bool kInt8, bool kFp8>
-static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, int n_pairs, cudaStream_t stream) {
+static cudaError_t configure(int dev) {
   using L = Layout<kInt8>;
   static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(segment_attn_kernel<kInt8, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAlloc);
+    const cudaError_t e = cudaFuncSetAttribute(segment_attn_kernel<kInt8, kFp8>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+template <bool kInt8, bool kFp8>
+static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, int n_items, cudaStream_t stream) {
+  using L = Layout<kInt8>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = configure<kInt8, kFp8>(dev);
+  if (e != cudaSuccess) return e;
   if constexpr (kInt8) {
     // CTA pairs (clusters of two adjacent query blocks) share the dequantised
-    // tiles; an odd count gets one query block past the end (no live rows).
+    // tiles; the second block of a pair may lie past the end (no live rows).
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((n_pairs + 1) & ~1, p.heads, p.num_splits);
+    cfg.gridDim = dim3(2u * static_cast<unsigned>(n_items), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = L::kAlloc;
     cfg.stream = stream;
@@ -750,29 +808,74 @@ static cudaError_t launch_impl(const AttnTensorMaps& tm, const AttnParams& p, in
     e = cudaLaunchKernelEx(&cfg, segment_attn_kernel<kInt8, kFp8>, tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
     if (e != cudaSuccess) return e;
   } else {
-    dim3 grid(n_pairs, p.heads, p.num_splits);
-    segment_attn_kernel<kInt8, kFp8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc,
-                                                                             p);
+    segment_attn_kernel<kInt8, kFp8><<<static_cast<unsigned>(n_items), kThreads, L::kAlloc, stream>>>(
+        tm.q, tm.kcur, tm.vcur, tm.kc, tm.vc, p);
   }
   return cudaGetLastError();
 }
 
+// Co-resident work items: one CTA per SM (BF16), or the number of clusters of
+// two CTAs that fit at once (one-byte caches).
+template <bool kInt8, bool kFp8>
+static int concurrent_items() {
+  using L = Layout<kInt8>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cached[64] = {0};
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
+  int n = sms;
+  if constexpr (kInt8) {
+    n = sms / 2;
+    if (configure<kInt8, kFp8>(dev) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2u * static_cast<unsigned>(sms), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = L::kAlloc;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, segment_attn_kernel<kInt8, kFp8>, &cfg) == cudaSuccess &&
+          clusters > 0)
+        n = clusters;
+      else
+        (void)cudaGetLastError();
+    }
+  }
+  cached[dev] = n;
+  return n;
+}
+
 }  // namespace attn
 
-cudaError_t launch_segment_attn(int kind, const AttnTensorMaps& tm, const AttnParams& p, int n_pairs,
+cudaError_t launch_segment_attn(int kind, const AttnTensorMaps& tm, const AttnParams& p, int n_items,
                                 cudaStream_t stream) {
-  if (kind == kCacheInt8) return attn::launch_impl<true, false>(tm, p, n_pairs, stream);
-  if (kind == kCacheFp8) return attn::launch_impl<true, true>(tm, p, n_pairs, stream);
-  if (kind == kCacheBF16) return attn::launch_impl<false, false>(tm, p, n_pairs, stream);
+  if (kind == kCacheInt8) return attn::launch_impl<true, false>(tm, p, n_items, stream);
+  if (kind == kCacheFp8) return attn::launch_impl<true, true>(tm, p, n_items, stream);
+  if (kind == kCacheBF16) return attn::launch_impl<false, false>(tm, p, n_items, stream);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream) {
-  const long long warps = static_cast<long long>(p.heads) * p.nq;
+cudaError_t launch_attn_combine(const AttnParams& p, int units, int ctas_per_unit, cudaStream_t stream) {
+  const int n_split_units = units - p.n_full;
+  if (p.tail_splits <= 1 || n_split_units <= 0) return cudaSuccess;
+  const long long warps = static_cast<long long>(n_split_units) * ctas_per_unit * 256;
   const long long blocks = (warps * 32 + 255) / 256;
-  attn::combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.ws_o, p.ws_lse, p.num_splits, p.heads,
-                                                                          p.nq, p.out, p.lse);
+  attn::combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p, n_split_units, ctas_per_unit);
   return cudaGetLastError();
+}
+
+int attn_concurrent_items(int kind) {
+  if (kind == kCacheInt8) return attn::concurrent_items<true, false>();
+  if (kind == kCacheFp8) return attn::concurrent_items<true, true>();
+  return attn::concurrent_items<false, false>();
 }
 
 int attn_smem_bytes(bool int8_cache) {

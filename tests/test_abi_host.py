@@ -128,15 +128,64 @@ def test_invalid_calls_return_status_without_launching():
     assert nomas.nomas_kvcache_append(ctypes.byref(d), None, None, nomas.NOMAS_BF16, 0, 0, None) == nomas.NOMAS_OK
 
 
+def _round256(x):
+    return -(-x // 256) * 256
+
+
 def test_workspace_bytes_for_explicit_splits():
+    # INT8 window of 18 frames, 7360 + 256 queries: 30 blocks of 256 rows per
+    # head form 15 CTA-pair units, 240 units in all.  Four pieces of every unit
+    # keep float32 partial rows of 128 values plus a log-sum-exp per piece, per
+    # CTA of the pair, per row of its 256-row block.
     d = _desc(heads=16, gh=23, gw=40, cap=18, past=18, total=24, valid=18)
     out = ctypes.c_size_t()
     assert nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), 7360, 256, 1, out) == nomas.NOMAS_OK
     assert out.value == 0
     assert nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), 7360, 256, 4, out) == nomas.NOMAS_OK
-    nq = 7616
-    want = -(-4 * 16 * nq * 128 * 4 // 256) * 256 + -(-4 * 16 * nq * 4 // 256) * 256
-    assert out.value == want
+    rows = 16 * 15 * 4 * 2 * 256
+    assert out.value == _round256(rows * 128 * 4) + _round256(rows * 4)
+    pl = nomas.nomas_attn_plan()
+    assert nomas.nomas_segment_attn_plan(ctypes.byref(d), 7360, 256, 4, ctypes.byref(pl)) == nomas.NOMAS_OK
+    assert (pl.units, pl.whole_units, pl.pieces_per_split_unit, pl.ctas_per_unit) == (240, 0, 4, 2)
+    assert pl.work_items == 960 and pl.workspace_bytes == out.value
+
+
+@pytest.mark.parametrize("dtype,frames,cur,slots", [
+    (nomas.NOMAS_BF16, 60, 8, 148),   # 60-frame BF16 history: 16 x 30 units of 256 rows
+    (nomas.NOMAS_INT8, 18, 8, 74),    # INT8 window of 18 frames: 16 x 15 CTA-pair units
+    (nomas.NOMAS_BF16, 8, 4, 148),    # 8-frame BF16 history, 4-frame segment: 16 x 16 units
+])
+def test_automatic_plan_is_consistent(dtype, frames, cur, slots):
+    # Without a GPU the plan assumes a full B300 (148 SMs, 74 CTA pairs).  The
+    # whole units fill whole waves; the pieces of the split units make a
+    # complete work list; the workspace holds exactly their partial rows.
+    past = frames if dtype == nomas.NOMAS_INT8 else 0
+    d = _desc(heads=16, gh=23, gw=40, cap=max(frames, 68), dtype=dtype, past=past, total=frames, valid=frames)
+    if past:
+        d.capacity_frames = frames
+    assert nomas.nomas_kvcache_validate(ctypes.byref(d)) == nomas.NOMAS_OK
+    nv = cur * 920
+    pl = nomas.nomas_attn_plan()
+    assert nomas.nomas_segment_attn_plan(ctypes.byref(d), nv, 256, 0, ctypes.byref(pl)) == nomas.NOMAS_OK
+    ctas = 2 if dtype == nomas.NOMAS_INT8 else 1
+    blocks = -(-(nv + 256) // 256)
+    assert pl.ctas_per_unit == ctas and pl.units == 16 * -(-blocks // ctas)
+    split_units = pl.units - pl.whole_units
+    assert pl.work_items == pl.whole_units + split_units * pl.pieces_per_split_unit
+    if pl.pieces_per_split_unit == 1:
+        assert split_units == 0 and pl.workspace_bytes == 0
+    else:
+        assert pl.whole_units % slots == 0
+        rows = split_units * pl.pieces_per_split_unit * ctas * 256
+        assert pl.workspace_bytes == _round256(rows * 512) + _round256(rows * 4)
+    out = ctypes.c_size_t()
+    assert nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), nv, 256, 0, out) == nomas.NOMAS_OK
+    assert out.value == pl.workspace_bytes
+    if frames >= 18:
+        # the two long-history shapes: 3 whole waves, the 36 (BF16) or 18
+        # (pair) units of the fourth wave cut into pieces that run as one wave
+        assert pl.whole_units == 3 * slots and split_units * pl.pieces_per_split_unit <= slots
+        assert pl.pieces_per_split_unit >= 2
 
 
 def test_archive_frame_bytes_matches_the_archive_growth_on_the_page():

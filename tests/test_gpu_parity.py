@@ -183,20 +183,68 @@ def test_attention_ragged_shapes(case, splits):
     assert_attn_close(out, ref_o, lse, ref_lse)
 
 
-def _sample_rows(n_q, n_video, seed):
+@pytest.mark.parametrize("case", range(len(RAGGED)))
+def test_attention_tail_plans(case):
+    # Plans that keep some units whole and cut the rest into pieces (the shape
+    # the automatic plan takes on long histories), on ragged shapes.
+    wl = small_variant(CONFIGS["c2_bf16_hist8"], **RAGGED[case], seed=200 + case)
+    gc, oc = build_caches(wl)
+    q, k, v = current_qkv(wl)
+    ref_o, ref_lse = oracle_segment(wl, oc, q, k, v)
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+    units = gc.attn_plan(wl.n_video, wl.n_text, 1)["units"]
+    n_tiles = -(-wl.n_cache // 128) + -(-wl.n_q // 128)
+    for whole, pieces in ((units - 1, 2), (max(0, units - 3), min(3, n_tiles)), (1, n_tiles), (0, 2)):
+        if whole >= units or pieces < 2 or pieces > n_tiles:
+            continue
+        lse = torch.empty((wl.heads, wl.n_q), dtype=torch.float32, device="cuda")
+        out = nomas.segment_attn_planned(gc, 0, qd, kd, vd, wl.n_video, wl.n_text, whole, pieces, lse=lse)
+        assert_attn_close(out, ref_o, lse, ref_lse)
+
+
+def _tile_rows(n_q, seed, per_tile=6):
+    """At least ``per_tile`` query rows from every 128-row tile (its first and last row among them)."""
     rng = np.random.default_rng(seed)
-    rows = set(rng.choice(n_q, size=min(n_q, 80), replace=False).tolist())
-    rows |= {0, 127, 128, 255, 256, n_video - 1, n_video, n_q - 1}
-    return np.array(sorted(r for r in rows if 0 <= r < n_q))
+    rows = set()
+    for t0 in range(0, n_q, 128):
+        t1 = min(n_q, t0 + 128)
+        rows |= {t0, t1 - 1}
+        rows |= set(rng.integers(t0, t1, size=per_tile - 2).tolist())
+    return np.array(sorted(rows))
 
 
-@pytest.mark.parametrize("name", ["c2_bf16_hist8", "c3_int8_window18", "c4_bf16_hist60"])
-def test_attention_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["c2_bf16_hist8", "c3_int8_window18"])
+def test_attention_full_size_every_row(name):
+    # Every query row of every head, against the oracle, under the automatic
+    # plan (a cut last wave on the INT8 window), an uncut plan, and a plan
+    # with a cut tail forced on the BF16 history.
     wl = CONFIGS[name]
     gc, oc = build_caches(wl)
     q, k, v = current_qkv(wl)
-    rows = _sample_rows(wl.n_q, wl.n_video, wl.seed)
+    ref_o, ref_lse = oracle_segment(wl, oc, q, k, v)
+    out, lse = gpu_segment(wl, gc, q, k, v, num_splits=0)
+    assert_attn_close(out, ref_o, lse, ref_lse)
+    out1, lse1 = gpu_segment(wl, gc, q, k, v, num_splits=1)
+    assert_attn_close(out1, ref_o, lse1, ref_lse)
+    if wl.cache_dtype == "bf16":
+        qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+        nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        lse2 = torch.empty_like(lse)
+        out2 = nomas.segment_attn_planned(gc, 0, qd, kd, vd, wl.n_video, wl.n_text, 148, 4, lse=lse2)
+        assert_attn_close(out2, ref_o, lse2, ref_lse)
+
+
+def test_attention_full_size_every_tile_c4():
+    # The 60-frame BF16 history: six rows of every 128-row query tile of every
+    # head (the oracle's cost bounds the sample), automatic and uncut plans.
+    wl = CONFIGS["c4_bf16_hist60"]
+    gc, oc = build_caches(wl)
+    q, k, v = current_qkv(wl)
+    rows = _tile_rows(wl.n_q, wl.seed)
     ref_o, ref_lse = oracle_segment(wl, oc, q, k, v, rows=rows)
+    plan = gc.attn_plan(wl.n_video, wl.n_text, 0)
+    assert plan["pieces_per_split_unit"] > 1 and plan["whole_units"] > 0
     out, lse = gpu_segment(wl, gc, q, k, v, num_splits=0)
     assert_attn_close(out, ref_o, lse, ref_lse, rows=rows)
     out1, _ = gpu_segment(wl, gc, q, k, v, num_splits=1)
