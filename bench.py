@@ -119,7 +119,8 @@ def whole_job_value(flops_per_step: float, world: int, steps: int, total_ms: flo
 
 
 def hbm_entry(nbytes: float, us: float, hbm_gbs: float, launches: int, **extra) -> dict:
-    """Bandwidth summary of an HBM-bound kernel group: algorithmic bytes over its event time."""
+    """Bandwidth summary of an HBM-bound kernel group: algorithmic bytes over its event time (inside
+    the step unless ``timing`` says otherwise)."""
     gbs = nbytes / (us * 1e-6) / 1e9 if us > 0 else None
     d = {"bound": "hbm", "algorithmic_bytes": int(nbytes), "us": us, "achieved": gbs, "peak": hbm_gbs,
          "unit": "GB/s", "frac": gbs / hbm_gbs if gbs else None,
@@ -252,40 +253,65 @@ class ClockSampler:
         self.source = None
         self.nvml_error = None
 
-    def _nvml_handle(self):
-        import pynvml
-        pynvml.nvmlInit()
-        import torch
-        props = torch.cuda.get_device_properties(self.device)
-        tries = []
-        uuid = str(getattr(props, "uuid", ""))
-        if uuid:
-            tries.append(lambda: pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid))
-        if hasattr(props, "pci_bus_id"):
-            bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
-            tries.append(lambda: pynvml.nvmlDeviceGetHandleByPciBusId(bus))
-        if pynvml.nvmlDeviceGetCount() == 1 or "CUDA_VISIBLE_DEVICES" not in os.environ:
-            tries.append(lambda: pynvml.nvmlDeviceGetHandleByIndex(self.device.index or 0))
-        errors = []
-        for t in tries:
+    class _Nvml:
+        """The few NVML calls the sampler needs, through ctypes on the driver's libnvidia-ml."""
+
+        def __init__(self):
+            import ctypes
+            self.ct = ctypes
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+
+        def _ok(self, rc, what):
+            if rc != 0:
+                raise RuntimeError(f"{what} returned {rc}")
+
+        def handle(self, device):
+            ct = self.ct
+            h = ct.c_void_p()
+            errors = []
             try:
-                return pynvml, t()
-            except Exception as e:  # try the next way of naming the device
+                import torch
+                uuid = str(torch.cuda.get_device_properties(device).uuid)
+                if uuid:
+                    u = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid).encode()
+                    if self.lib.nvmlDeviceGetHandleByUUID(ct.c_char_p(u), ct.byref(h)) == 0:
+                        return h
+                    errors.append("uuid " + uuid)
+            except Exception as e:  # fall back to the index
                 errors.append(repr(e))
-        raise RuntimeError("no NVML handle: " + "; ".join(errors))
+            n = ct.c_uint(0)
+            self._ok(self.lib.nvmlDeviceGetCount_v2(ct.byref(n)), "nvmlDeviceGetCount_v2")
+            if n.value == 1 or "CUDA_VISIBLE_DEVICES" not in os.environ:
+                self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(device.index or 0), ct.byref(h)),
+                         "nvmlDeviceGetHandleByIndex_v2")
+                return h
+            raise RuntimeError("no NVML handle: " + "; ".join(errors))
+
+        def sample(self, h):
+            ct = self.ct
+            sm, smax = ct.c_uint(0), ct.c_uint(0)
+            util = (ct.c_uint * 2)()
+            reasons = ct.c_ulonglong(0)
+            self._ok(self.lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(sm)), "nvmlDeviceGetClockInfo")  # 1 = SM clock
+            self._ok(self.lib.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(smax)), "nvmlDeviceGetMaxClockInfo")
+            self._ok(self.lib.nvmlDeviceGetUtilizationRates(h, util), "nvmlDeviceGetUtilizationRates")
+            fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._ok(fn(h, ct.byref(reasons)), "clock event reasons")
+            return float(sm.value), float(smax.value), float(util[0]), int(reasons.value)
 
     def start(self):
         try:
-            nv, h = self._nvml_handle()
-            smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+            nv = self._Nvml()
+            h = nv.handle(self.device)
+            nv.sample(h)
 
             def loop():
                 while not self.stop_flag.is_set():
                     try:
-                        sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                        busy = nv.nvmlDeviceGetUtilizationRates(h).gpu
-                        rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-                        self.samples.append((float(sm), float(smax), float(busy), int(rs)))
+                        self.samples.append(nv.sample(h))
                     except Exception:
                         pass
                     self.stop_flag.wait(0.01)
@@ -492,8 +518,8 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
     # sit between steps, outside them, and the sleep precedes the first step.
     torch.cuda._sleep(int(2e6) * steps)
     for i in range(steps):
-        evict_l2()  # untimed, between steps
-        restage()
+        restage()   # untimed, between steps: fresh inputs, then L2 evicted so they start in HBM
+        evict_l2()
         evs[i][0].record(stream)
         step(evs[i][2:])
         evs[i][1].record(stream)
@@ -502,6 +528,26 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
+    # The append group and RoPE each on their own after an L2 eviction (their
+    # inputs in HBM, no other kernel's dirty lines to write back): the
+    # kernels' own bandwidth, next to their times inside the step.
+    iso = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(min(steps, 50))]
+    for ev in iso:
+        restage()
+        cache.reset(zero_memory=False)
+        evict_l2()
+        ev[0].record(stream)
+        for kh, vh in hist_d:
+            if args.append_rope:
+                cache.append_rope(kh, vh, wl.theta, wl.rope_split)
+            else:
+                cache.append(kh, vh)
+        ev[1].record(stream)
+        evict_l2()
+        ev[2].record(stream)
+        nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        ev[3].record(stream)
+    torch.cuda.synchronize(dev)
     r = {
         "step_ms": [e[0].elapsed_time(e[1]) for e in evs],
         "append_ms": [e[2].elapsed_time(e[3]) for e in evs],
@@ -510,6 +556,8 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
         "select_ms": [e[8].elapsed_time(e[9]) for e in evs] if keep else None,
         "camera_ms": [e[10].elapsed_time(e[11]) for e in evs] if camera else None,
         "clocks": clocks, "plan": plan, "hist": hist, "qkv": (q_h, k_h, v_h), "steps": steps,
+        "append_iso_ms": [e[0].elapsed_time(e[1]) for e in iso],
+        "rope_iso_ms": [e[2].elapsed_time(e[3]) for e in iso],
     }
     r["flops"] = sparse_flops(wl, sel_tiles.cpu().numpy(), sel_counts.cpu().numpy()) if keep else wl.attn_flops()
     r["launches_per_step"] = (len(hist) + 1 + 1 + (1 if plan["pieces_per_split_unit"] > 1 else 0)
@@ -529,8 +577,12 @@ def summarize_block_call(wl, m, world, steps, peaks, append_rope=False, camera=0
     achieved = m["flops"] / (attn_avg * 1e-3) / 1e12
     el = {}
     name = "kvcache_append_rope" if append_rope else "kvcache_append"
-    el[name] = hbm_entry(append_bytes(wl), 1e3 * statistics.mean(m["append_ms"]), hbm, len(wl.cache_frames_hist))
-    el["rope3d"] = hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_ms"]), hbm, 1)
+    el[name] = hbm_entry(append_bytes(wl), 1e3 * statistics.mean(m["append_ms"]), hbm, len(wl.cache_frames_hist),
+                         isolated=hbm_entry(append_bytes(wl), 1e3 * statistics.median(m["append_iso_ms"]), hbm,
+                                            len(wl.cache_frames_hist), timing="alone after an L2 eviction"))
+    el["rope3d"] = hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_ms"]), hbm, 1,
+                             isolated=hbm_entry(rope_bytes(wl), 1e3 * statistics.median(m["rope_iso_ms"]), hbm, 1,
+                                                timing="alone after an L2 eviction"))
     if camera:
         nbytes = 2 * wl.n_video * wl.heads * wl.head_dim * 2 + 2 * wl.cur_frames * camera * wl.heads * wl.head_dim * 2
         el["camera_cross_attn"] = hbm_entry(nbytes, 1e3 * statistics.mean(m["camera_ms"]), hbm, 1,
@@ -760,14 +812,19 @@ def _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world):
     return res
 
 
-ATTN_SOURCES = ("segment_causal_kv_int8_b300/csrc/segment_attn.cu", "segment_causal_kv_int8_b300/csrc/sm100.cuh")
+_CSRC = "segment_causal_kv_int8_b300/csrc/"
+ATTN_SOURCES = {  # the kernel a cache format runs, with the headers it includes
+    "bf16": tuple(_CSRC + f for f in ("segment_attn.cu", "attn_common.cuh", "sm100.cuh", "checks.cuh")),
+    "int8": tuple(_CSRC + f for f in ("segment_attn_pair.cu", "attn_common.cuh", "sm100.cuh", "checks.cuh")),
+}
+ATTN_SOURCES["fp8"] = ATTN_SOURCES["int8"]
 
 
-def attn_source_hash() -> str:
+def attn_source_hash(cache_dtype: str = "bf16") -> str:
     """sha256 over the attention kernel's sources (decides whether committed counters still apply)."""
     import hashlib
     h = hashlib.sha256()
-    for rel in ATTN_SOURCES:
+    for rel in ATTN_SOURCES[cache_dtype]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -791,7 +848,8 @@ def _load_traffic(config):
                     fields[k.strip(" `")] = v.strip(" `")
     except OSError:
         return None, f"no ncu capture committed ({rel} missing)"
-    if fields.get("kernel_source_sha256") != attn_source_hash():
+    from synth import CONFIGS
+    if fields.get("kernel_source_sha256") != attn_source_hash(CONFIGS[config].cache_dtype):
         return None, f"{rel} was captured from other kernel sources (hash differs)"
     try:
         return int(float(fields["dram_bytes_per_launch"])), (

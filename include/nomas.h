@@ -441,6 +441,24 @@ nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStre
 nomas_status nomas_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
 /*
+ * The range-checked build (no counterpart in the pages).  The library also
+ * ships as libnomas_checked.so, the same kernels compiled so that every
+ * computed global-memory index (TMA tile origins, ring slots, cache rows and
+ * scales, tile-list entries, output, partial and workspace rows) is checked
+ * against its buffer before the access: a bad index records
+ * NOMAS_ERR_INVALID_ARG in the device error word and the access is skipped;
+ * nothing traps.
+ *
+ * nomas_bounds_checked: 1 in the checked build, 0 otherwise.
+ * nomas_selftest_bounds_check: checked build only, enqueue a one-warp kernel
+ * whose single range check fails on purpose (index 4 of a 4-element buffer),
+ * so NOMAS_ERR_INVALID_ARG lands in the device error word with no access made.
+ * Returns NOMAS_ERR_UNSUPPORTED, launching nothing, in the regular build.
+ */
+int32_t nomas_bounds_checked(void);
+nomas_status nomas_selftest_bounds_check(cudaStream_t stream);
+
+/*
  * Read the device-side error word of the current device (a status code set
  * by a kernel that gave up waiting, 0 if none), synchronously.  With clear != 0
  * the word is reset to 0.  *status receives NOMAS_OK or the recorded status.

@@ -8,8 +8,11 @@ conveniences over them that take torch tensors and raise :class:`NomasError`
 on any status other than ``NOMAS_OK``.
 
 There is no CPU fallback: importing this package loads the shared library and
-fails loudly when it has not been built (``python -m
-segment_causal_kv_int8_b300/_build.py``).
+fails loudly when it has not been built (``python
+segment_causal_kv_int8_b300/_build.py``).  With ``NOMAS_LIBRARY=checked`` in the
+environment it loads ``libnomas_checked.so`` instead: the same kernels with every
+computed global-memory index range-checked (a bad index is recorded in the
+device error word as NOMAS_ERR_INVALID_ARG and its access skipped).
 """
 from __future__ import annotations
 
@@ -19,7 +22,10 @@ import os
 from typing import Optional
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libnomas.so")
+_VARIANT = os.environ.get("NOMAS_LIBRARY", "")
+if _VARIANT not in ("", "checked"):
+    raise ImportError(f"NOMAS_LIBRARY={_VARIANT!r}: expected unset or 'checked'")
+LIB_PATH = os.path.join(_PKG, "libnomas_checked.so" if _VARIANT == "checked" else "libnomas.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -113,6 +119,8 @@ EXPORTS = {
     "nomas_camera_cross_attn": (_c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
     "nomas_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _vp]),
+    "nomas_bounds_checked": (_i32, []),
+    "nomas_selftest_bounds_check": (_c_int, [_vp]),
     "nomas_device_error": (_c_int, [_P(_c_int), _c_int]),
 }
 

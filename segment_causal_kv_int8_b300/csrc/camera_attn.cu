@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 
 namespace nomas {
@@ -61,7 +62,9 @@ __global__ void __launch_bounds__(256) camera_attn_kernel(const __grid_constant_
   for (int r = 0; r < kCamRowsPerGroup; ++r) {
     const int tok = tok0 + 4 * r;
     qw[r] = make_uint4(0u, 0u, 0u, 0u);
-    if (tok < p.tpf && hh < nh)
+    if (tok < p.tpf && hh < nh &&
+        in_bounds(((static_cast<long long>(f) * p.tpf + tok) * p.heads + h0 + hh) * 128 + 8 * g, 8,
+                  static_cast<long long>(p.frames) * p.tpf * p.heads * 128, p.err))
       qw[r] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                              ((static_cast<size_t>(f) * p.tpf + tok) * p.heads + h0 + hh) * 128)[g];
   }
@@ -70,7 +73,8 @@ __global__ void __launch_bounds__(256) camera_attn_kernel(const __grid_constant_
     const int kv = i / cam_vecs, r = i - kv * cam_vecs;
     const int j = r / (kCamHeads * 16), ch = (r / 16) % kCamHeads, c = r % 16;
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (ch < nh) {
+    if (ch < nh && in_bounds(((static_cast<long long>(f) * p.n_cam + j) * p.heads + h0 + ch) * 128 + 8 * c, 8,
+                             static_cast<long long>(p.frames) * p.n_cam * p.heads * 128, p.err)) {
       const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(kv ? p.v_cam : p.k_cam);
       w = reinterpret_cast<const uint4*>(src + ((static_cast<size_t>(f) * p.n_cam + j) * p.heads + h0 + ch) * 128)[c];
     }
@@ -118,7 +122,9 @@ __global__ void __launch_bounds__(256) camera_attn_kernel(const __grid_constant_
 #pragma unroll
   for (int r = 0; r < kCamRowsPerGroup; ++r) {
     const int tok = tok0 + 4 * r;
-    if (tok < p.tpf && hh < nh) {
+    if (tok < p.tpf && hh < nh &&
+        in_bounds(((static_cast<long long>(f) * p.tpf + tok) * p.heads + h0 + hh) * 128 + 8 * g, 8,
+                  static_cast<long long>(p.frames) * p.tpf * p.heads * 128, p.err)) {
       const float inv = 1.0f / l[r];
       uint4 w;
       uint32_t* u = reinterpret_cast<uint32_t*>(&w);

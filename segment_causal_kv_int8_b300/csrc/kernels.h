@@ -67,6 +67,8 @@ cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);
 
 // ------------------------------------------------------------------ self-test
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
+bool bounds_checked_build();
+cudaError_t launch_bounds_check_selftest(uint32_t* err, cudaStream_t stream);
 
 // ------------------------------------------------------------------ sparse selection
 struct SparseSelectParams {
@@ -85,6 +87,8 @@ struct SparseSelectParams {
   float* kbar;                   // workspace [heads][n_tiles][128]
   int* tiles;                    // [heads][n_groups][max_keep]
   int* counts;                   // [heads][n_groups]
+  long long cache_rows;          // blocks * heads * cap_slots (checked build)
+  uint32_t* err;                 // device error word (checked build)
 };
 
 size_t sparse_select_smem(int n_tiles);
@@ -102,6 +106,7 @@ struct CameraAttnParams {
   int heads;
   int n_cam;                     // camera tokens per latent frame, 1 .. 16
   float scale_log2;              // softmax scale * log2(e)
+  uint32_t* err;                 // device error word (checked build)
 };
 
 cudaError_t launch_camera_attn(const CameraAttnParams& p, cudaStream_t stream);

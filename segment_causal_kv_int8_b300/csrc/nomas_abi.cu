@@ -499,6 +499,8 @@ NOMAS_API nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam,
   p.heads = heads;
   p.n_cam = n_cam;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.err = nullptr;
+  if (device_state(&p.err, nullptr) != NOMAS_OK) p.err = nullptr;
   return from_cuda(launch_camera_attn(p, stream));
 }
 
@@ -748,6 +750,9 @@ NOMAS_API nomas_status nomas_sparse_select(const nomas_kvcache* cache, int32_t b
   p.kbar = static_cast<float*>(workspace);
   p.tiles = tiles;
   p.counts = counts;
+  p.cache_rows = static_cast<long long>(cache->num_blocks) * cache->heads * p.cap_slots;
+  p.err = nullptr;
+  if (device_state(&p.err, nullptr) != NOMAS_OK) p.err = nullptr;
   if (n_tiles == 0) {
     // Nothing resident: every list is empty.
     return from_cuda(cudaMemsetAsync(counts, 0, static_cast<size_t>(cache->heads) * n_groups * 4, stream));
@@ -773,6 +778,16 @@ NOMAS_API nomas_status nomas_selftest_wait_timeout(uint32_t limit_us, cudaStream
   nomas_status st = device_state(&err, nullptr);
   if (st != NOMAS_OK) return st;
   return from_cuda(launch_wait_timeout_selftest(err, static_cast<uint64_t>(limit_us) * 1000ull, stream));
+}
+
+NOMAS_API int32_t nomas_bounds_checked(void) { return bounds_checked_build() ? 1 : 0; }
+
+NOMAS_API nomas_status nomas_selftest_bounds_check(cudaStream_t stream) {
+  if (!bounds_checked_build()) return NOMAS_ERR_UNSUPPORTED;
+  uint32_t* err = nullptr;
+  nomas_status st = device_state(&err, nullptr);
+  if (st != NOMAS_OK) return st;
+  return from_cuda(launch_bounds_check_selftest(err, stream));
 }
 
 NOMAS_API nomas_status nomas_device_error(nomas_status* status, int clear) {

@@ -7,13 +7,14 @@
 //
 // HBM-bound elementwise kernel.  Each CTA takes a contiguous run of tokens:
 // it first computes the cos/sin of every (token, pair) of the run once into
-// shared memory (angle arithmetic in rope_math.cuh), then streams the rows of
-// Q and K as 16-byte vectors, one vector per thread per tensor and token, two
-// tokens in flight per thread.  The grid is one resident wave of CTAs with
-// equal token runs, so no partial last wave.  A thread's vectors always hold
-// the same rotary pairs, so its table reads are two consecutive 16-byte
-// loads.  The cos/sin of a pair depend only on its position and frequency, so
-// the rotation is bit for bit what per-element evaluation gives.
+// shared memory (angle arithmetic in rope_math.cuh; shared by every head and
+// by Q and K), then streams the rows of Q and K as 16-byte vectors, one
+// vector per thread per tensor and token, four tokens in flight per thread
+// (eight loads).  The grid is one resident wave of CTAs with equal token
+// runs, so no partial last wave.  A thread's vectors always hold the same
+// rotary pairs, so its table reads are one or two 16-byte loads.  The cos/sin
+// of a pair depend only on its position and frequency, so the rotation is bit
+// for bit what per-element evaluation gives.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -26,104 +27,6 @@
 
 namespace nomas {
 namespace {
-
-constexpr int kRopeHeadsPerThread = 4;
-
-// Rotate one 8-value group (4 pairs) held as floats.
-__device__ __forceinline__ void rotate8(float (&x)[8], const float (&cs)[4], const float (&sn)[4]) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) rope_rotate_pair(x[2 * e], x[2 * e + 1], cs[e], sn[e]);
-}
-
-// Block: 16 tokens x 16 lanes (a lane owns 4 consecutive rotary pairs, i.e. 8
-// values, of every head row); blockIdx.y picks a group of kRopeHeadsPerThread
-// heads.  All loads of a thread (its heads of Q and K) are issued before any
-// arithmetic so enough bytes are in flight to keep HBM busy.
-template <bool kBF16>
-__global__ void __launch_bounds__(256) rope3d_kernel(void* __restrict__ q, void* __restrict__ k,
-                                                     const __grid_constant__ RopeParams p, TwoPi tp) {
-  constexpr int HT = kRopeHeadsPerThread;
-  const int g = threadIdx.x & 15;
-  const int tok = blockIdx.x * 16 + (threadIdx.x >> 4);
-  if (tok >= p.n_video) return;
-  const int h0 = blockIdx.y * HT;
-  const int nh = min(HT, p.heads - h0);
-  bool any = false;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) any |= p.axis[4 * g + e] >= 0;
-  if (!any) return;
-  if (!in_bounds(static_cast<long long>(tok) * p.row_stride + h0 * 128 + 8 * g, (nh - 1) * 128 + 8, p.extent, p.err))
-    return;
-  const int nt = (k != nullptr) ? 2 : 1;
-  using Vec = typename std::conditional<kBF16, uint4, float4>::type;
-  constexpr int kVecs = kBF16 ? 1 : 2;  // 16-byte vectors per 8-value group
-  Vec w[2][HT][kVecs];
-#pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    if (which >= nt) break;
-    const Vec* row = reinterpret_cast<const Vec*>(static_cast<const char*>(which ? k : q) +
-                                                  (static_cast<long long>(tok) * p.row_stride + h0 * 128 + 8 * g) * (kBF16 ? 2 : 4));
-#pragma unroll
-    for (int u = 0; u < HT; ++u)
-      if (u < nh)
-#pragma unroll
-        for (int c = 0; c < kVecs; ++c) w[which][u][c] = row[u * (128 * (kBF16 ? 2 : 4) / 16) + c];
-  }
-  const int frame = tok / p.tpf;
-  const int within = tok - frame * p.tpf;
-  const int row = within / p.grid_w;
-  const float pos[3] = {static_cast<float>(p.t0 + frame), static_cast<float>(row),
-                        static_cast<float>(within - row * p.grid_w)};
-  float cs[4], sn[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int pair = 4 * g + e;
-    const int a = p.axis[pair];
-    if (a < 0) {
-      cs[e] = 1.0f;
-      sn[e] = 0.0f;
-    } else {
-      sincosf(rope_reduced_angle(pos[a], p.f_hi[pair], p.f_lo[pair], tp), &sn[e], &cs[e]);
-    }
-  }
-#pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    if (which >= nt) break;
-    Vec* row = reinterpret_cast<Vec*>(static_cast<char*>(which ? k : q) +
-                                      (static_cast<long long>(tok) * p.row_stride + h0 * 128 + 8 * g) * (kBF16 ? 2 : 4));
-#pragma unroll
-    for (int u = 0; u < HT; ++u) {
-      if (u >= nh) continue;
-      float x[8];
-      if constexpr (kBF16) {
-        const uint32_t* v = reinterpret_cast<const uint32_t*>(&w[which][u][0]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          x[2 * e] = __uint_as_float(v[e] << 16);
-          x[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
-        }
-      } else {
-        const float* v = reinterpret_cast<const float*>(&w[which][u][0]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = v[e];
-      }
-      rotate8(x, cs, sn);
-      if constexpr (kBF16) {
-        uint4 o;
-        uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 t2 = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-          ov[e] = *reinterpret_cast<const uint32_t*>(&t2);
-        }
-        row[u * 16] = o;
-      } else {
-        row[u * 32] = make_float4(x[0], x[1], x[2], x[3]);
-        row[u * 32 + 1] = make_float4(x[4], x[5], x[6], x[7]);
-      }
-    }
-  }
-}
 
 constexpr int kRunMax = 32;  // tokens of one table fill (32 x 64 pairs x 8 B = 16 KB of shared memory)
 
@@ -176,27 +79,29 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
     }
     __syncthreads();
     if (active && rotated) {
-      for (int tl = t_off; tl < nf; tl += 2 * tpi) {
-        const int tl1 = tl + tpi;
-        const bool two = tl1 < nf;
+      constexpr int U = 4;  // tokens in flight per thread
+      for (int tl = t_off; tl < nf; tl += U * tpi) {
         for (int rem = rem0; rem < V; rem += 256) {
           const int head = rem / VPR;
-          // element offset of this vector in token f0 + tl (and f0 + tl1)
-          const long long off0 = static_cast<long long>(f0 + tl) * p.row_stride + head * 128 + g * (16 / ESZ);
-          const long long off1 = off0 + static_cast<long long>(tpi) * p.row_stride;
-          if (!in_bounds(off0, 16 / ESZ, p.extent, p.err) || (two && !in_bounds(off1, 16 / ESZ, p.extent, p.err)))
-            continue;
-          Vec w[2][2];
+          long long off[U];
+          bool live[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            off[u] = static_cast<long long>(f0 + tl + u * tpi) * p.row_stride + head * 128 + g * (16 / ESZ);
+            live[u] = tl + u * tpi < nf && in_bounds(off[u], 16 / ESZ, p.extent, p.err);
+          }
+          Vec w[2][U];
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
             if (which >= nt) break;
             const Vec* base = reinterpret_cast<const Vec*>(static_cast<const char*>(which ? k : q));
-            w[which][0] = base[off0 * ESZ / 16];
-            if (two) w[which][1] = base[off1 * ESZ / 16];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (live[u]) w[which][u] = base[off[u] * ESZ / 16];
           }
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            if (u == 1 && !two) break;
+          for (int u = 0; u < U; ++u) {
+            if (!live[u]) continue;
             const float4* tab = reinterpret_cast<const float4*>(&cs[(tl + u * tpi) * 64 + g * PPV]);
             float cc[PPV], ss[PPV];
 #pragma unroll
@@ -230,7 +135,7 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
                 o = make_float4(x[0], x[1], x[2], x[3]);
               }
               Vec* base = reinterpret_cast<Vec*>(static_cast<char*>(which ? k : q));
-              base[(u ? off1 : off0) * ESZ / 16] = o;
+              base[off[u] * ESZ / 16] = o;
             }
           }
         }
@@ -245,34 +150,24 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream) {
   if (p.n_video <= 0) return cudaSuccess;
   const TwoPi tp = rope_two_pi();
-  // One resident wave of CTAs with equal token runs.
   int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
-    const cudaError_t e = bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<true>, 256, 0)
-                                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<false>, 256, 0);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();
-      per_sm = 0;
-    }
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  const cudaError_t e = bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<true>, 256, 0)
+                                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<false>, 256, 0);
+  if (e != cudaSuccess || per_sm <= 0) {
+    (void)cudaGetLastError();
+    per_sm = 4;
   }
-  if (per_sm > 0) {
-    const long long slots = static_cast<long long>(sms) * per_sm;
-    const int run = static_cast<int>((p.n_video + slots - 1) / slots);
-    const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);
-    if (bf16_io)
-      rope3d_run_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp, run);
-    else
-      rope3d_run_kernel<false><<<grid, 256, 0, stream>>>(q, k, p, tp, run);
-    return cudaGetLastError();
-  }
-  const dim3 grid(static_cast<unsigned>((p.n_video + 15) / 16),
-                  static_cast<unsigned>((p.heads + kRopeHeadsPerThread - 1) / kRopeHeadsPerThread));
-  if (grid.y > 65535) return cudaErrorInvalidValue;
+  // One resident wave of CTAs with equal token runs.
+  const long long slots = static_cast<long long>(sms) * per_sm;
+  const int run = static_cast<int>((p.n_video + slots - 1) / slots);
+  const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);
   if (bf16_io)
-    rope3d_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp);
+    rope3d_run_kernel<true><<<grid, 256, 0, stream>>>(q, k, p, tp, run);
   else
-    rope3d_kernel<false><<<grid, 256, 0, stream>>>(q, k, p, tp);
+    rope3d_run_kernel<false><<<grid, 256, 0, stream>>>(q, k, p, tp, run);
   return cudaGetLastError();
 }
 

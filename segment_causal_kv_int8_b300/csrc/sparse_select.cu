@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 
 namespace nomas {
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kSelThreads) tile_means_kernel(const SparseSel
 #pragma unroll
   for (int pass = 0; pass < 128 / kRowSlots; ++pass) {
     const int r = pass * kRowSlots + rs;
-    if (r < n) {
+    if (r < n && in_bounds(plane + r0 + r, 1, p.cache_rows, p.err)) {
       const long long row = plane + r0 + r;
       if constexpr (K == kCacheInt8) {
         const uint4 w = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(p.kcache) + row * 128)[c];
@@ -98,7 +99,8 @@ __global__ void __launch_bounds__(kSelThreads) tile_means_kernel(const SparseSel
   if (threadIdx.x < 128) {
     float s = 0.0f;
     for (int i = 0; i < kRowSlots; ++i) s += part[i][threadIdx.x];
-    p.kbar[(static_cast<size_t>(h) * p.n_tiles + t) * 128 + threadIdx.x] = s / static_cast<float>(n);
+    const long long idx = (static_cast<long long>(h) * p.n_tiles + t) * 128 + threadIdx.x;
+    if (in_bounds(idx, 1, static_cast<long long>(p.heads) * p.n_tiles * 128, p.err)) p.kbar[idx] = s / static_cast<float>(n);
   }
 }
 
@@ -134,7 +136,10 @@ __global__ void __launch_bounds__(kPickThreads, 2) select_kernel(const SparseSel
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = rs + 32 * (8 * half + i);
-        w[i] = r < n ? q[r * row_vecs] : make_uint4(0u, 0u, 0u, 0u);
+        w[i] = r < n && in_bounds((static_cast<long long>(r0 + r) * p.heads + h) * 128 + 8 * c, 8,
+                                  static_cast<long long>(p.nq) * p.heads * 128, p.err)
+                   ? q[r * row_vecs]
+                   : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) add_bf16x8(acc, w[i]);
@@ -222,7 +227,9 @@ __global__ void __launch_bounds__(kPickThreads, 2) select_kernel(const SparseSel
     int before = base;
     for (int w = 0; w < warp; ++w) before += s_warp[w];
     before += __popc(bal & ((1u << lane) - 1u));
-    if (k && before < p.keep) out[before] = t;
+    if (k && before < p.keep && in_bounds(static_cast<long long>(hg) * p.max_keep + before, 1,
+                                          static_cast<long long>(p.heads) * p.n_groups * p.max_keep, p.err))
+      out[before] = t;
     for (int w = 0; w < kPickThreads / 32; ++w) base += s_warp[w];
     __syncthreads();
   }

@@ -51,6 +51,34 @@ def test_rope3d_matches_oracle(name):
             assert np.all(d <= 2.0 ** -8 * np.abs(ref[:nv]) + ROPE_REL * vec_inf)
 
 
+@pytest.mark.parametrize("io_dtype", ["bf16", "f32"])
+def test_rope3d_padded_token_rows(io_dtype):
+    # Token rows farther apart than heads x 128 (Q and K viewed out of wider
+    # buffers): the kernel for strided rows, against the oracle; the padding
+    # between rows is left untouched.
+    wl = small_variant(CONFIGS["c2_bf16_hist8"], heads=3, grid_h=5, grid_w=7, cur_frames=3, n_text=4,
+                       io_dtype=io_dtype, seed=77)
+    q, k, _ = current_qkv(wl)
+    for src in (q, k):
+        wide = torch.full((wl.n_q, wl.heads + 2, 128), 7.0, dtype=torch.bfloat16 if io_dtype == "bf16" else
+                          torch.float32, device="cuda")
+        wide[:, :wl.heads] = to_dev(src, io_dtype)
+        view = wide[:, :wl.heads]
+        assert view.stride(0) == (wl.heads + 2) * 128
+        nomas.rope3d(view, None, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        ref = o_rope.rope3d_segment(src, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        got = f64(view)
+        nv = wl.n_video
+        np.testing.assert_array_equal(got[nv:], src[nv:].astype(np.float64))
+        d = np.abs(got[:nv] - ref[:nv])
+        vec_inf = np.max(np.abs(ref[:nv]), axis=2, keepdims=True)
+        if io_dtype == "f32":
+            assert np.max(np.max(d, axis=2, keepdims=True) / vec_inf) <= ROPE_REL
+        else:
+            assert np.all(d <= 2.0 ** -8 * np.abs(ref[:nv]) + ROPE_REL * vec_inf)
+        assert bool((wide[:, wl.heads:] == 7.0).all())
+
+
 def test_rope3d_large_frame_index_and_odd_split():
     wl = small_variant(CONFIGS["c1_tiny"], io_dtype="f32", grid_h=3, grid_w=5, cur_frames=3, n_text=2)
     q, k, _ = current_qkv(wl)
