@@ -813,18 +813,14 @@ def _e2e(args, torch, nomas, wl, hist, q_h, k_h, v_h, dev, world):
 
 
 _CSRC = "segment_causal_kv_int8_b300/csrc/"
-ATTN_SOURCES = {  # the kernel a cache format runs, with the headers it includes
-    "bf16": tuple(_CSRC + f for f in ("segment_attn.cu", "attn_common.cuh", "sm100.cuh", "checks.cuh")),
-    "int8": tuple(_CSRC + f for f in ("segment_attn_pair.cu", "attn_common.cuh", "sm100.cuh", "checks.cuh")),
-}
-ATTN_SOURCES["fp8"] = ATTN_SOURCES["int8"]
+ATTN_SOURCES = tuple(_CSRC + f for f in ("segment_attn.cu", "attn_common.cuh", "sm100.cuh", "checks.cuh"))
 
 
-def attn_source_hash(cache_dtype: str = "bf16") -> str:
+def attn_source_hash() -> str:
     """sha256 over the attention kernel's sources (decides whether committed counters still apply)."""
     import hashlib
     h = hashlib.sha256()
-    for rel in ATTN_SOURCES[cache_dtype]:
+    for rel in ATTN_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -848,8 +844,7 @@ def _load_traffic(config):
                     fields[k.strip(" `")] = v.strip(" `")
     except OSError:
         return None, f"no ncu capture committed ({rel} missing)"
-    from synth import CONFIGS
-    if fields.get("kernel_source_sha256") != attn_source_hash(CONFIGS[config].cache_dtype):
+    if fields.get("kernel_source_sha256") != attn_source_hash():
         return None, f"{rel} was captured from other kernel sources (hash differs)"
     try:
         return int(float(fields["dram_bytes_per_launch"])), (

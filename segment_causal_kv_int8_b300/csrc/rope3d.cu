@@ -9,9 +9,11 @@
 // it first computes the cos/sin of every (token, pair) of the run once into
 // shared memory (angle arithmetic in rope_math.cuh; shared by every head and
 // by Q and K), then streams the rows of Q and K as 16-byte vectors, one
-// vector per thread per tensor and token, four tokens in flight per thread
-// (eight loads).  The grid is one resident wave of CTAs with equal token
-// runs, so no partial last wave.  A thread's vectors always hold the same
+// vector per thread per tensor and token.  A thread works in items of two
+// tokens (four 16-byte loads) with two buffers: the first item's loads go out
+// before the table is computed, and each next item's loads are in flight
+// while the current one is rotated.  The grid is one resident wave of CTAs
+// with equal token runs, so no partial last wave.  A thread's vectors always hold the same
 // rotary pairs, so its table reads are one or two 16-byte loads.  The cos/sin
 // of a pair depend only on its position and frequency, so the rotation is bit
 // for bit what per-element evaluation gives.
@@ -59,8 +61,75 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
 #pragma unroll
   for (int e = 0; e < PPV; ++e) rotated |= axis_s[g * PPV + e] >= 0;
   const int nt = (k != nullptr) ? 2 : 1;
+  constexpr int U = 2;  // tokens of one item: U vectors of Q and U of K per thread
+  const int nrem = active ? (V - rem0 + 255) / 256 : 0;  // vectors of a token row this thread visits
+  // Item i of a fill: tokens t_off + (i / nrem) * U * tpi + u * tpi (u < U),
+  // vector rem0 + 256 * (i % nrem) of each token row.
+  auto locate = [&](int f0, int nf, int i, int u, int& tl, long long& off) {
+    const int a = i / nrem, b = i - (i / nrem) * nrem;
+    tl = t_off + a * U * tpi + u * tpi;
+    off = static_cast<long long>(f0 + tl) * p.row_stride + ((rem0 + 256 * b) / VPR) * 128 + g * (16 / ESZ);
+    return tl < nf && in_bounds(off, 16 / ESZ, p.extent, p.err);
+  };
+  auto load = [&](int f0, int nf, int i, Vec (&w)[2][U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int tl;
+      long long off;
+      if (!locate(f0, nf, i, u, tl, off)) continue;
+#pragma unroll
+      for (int which = 0; which < 2; ++which)
+        if (which < nt) w[which][u] = reinterpret_cast<const Vec*>(static_cast<const char*>(which ? k : q))[off * ESZ / 16];
+    }
+  };
+  auto rotate_store = [&](int f0, int nf, int i, const Vec (&w)[2][U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int tl;
+      long long off;
+      if (!locate(f0, nf, i, u, tl, off)) continue;
+      const float4* tab = reinterpret_cast<const float4*>(&cs[tl * 64 + g * PPV]);
+      float cc[PPV], ss[PPV];
+#pragma unroll
+      for (int h2 = 0; h2 < PPV / 2; ++h2) {
+        const float4 t4 = tab[h2];
+        cc[2 * h2] = t4.x;
+        ss[2 * h2] = t4.y;
+        cc[2 * h2 + 1] = t4.z;
+        ss[2 * h2 + 1] = t4.w;
+      }
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        if (which >= nt) break;
+        Vec o;
+        if constexpr (kBF16) {
+          const uint32_t* v = reinterpret_cast<const uint32_t*>(&w[which][u]);
+          uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x0 = __uint_as_float(v[e] << 16);
+            float x1 = __uint_as_float(v[e] & 0xFFFF0000u);
+            rope_rotate_pair(x0, x1, cc[e], ss[e]);
+            __nv_bfloat162 t2 = __floats2bfloat162_rn(x0, x1);
+            ov[e] = *reinterpret_cast<const uint32_t*>(&t2);
+          }
+        } else {
+          const float* v = reinterpret_cast<const float*>(&w[which][u]);
+          float x[4] = {v[0], v[1], v[2], v[3]};
+          rope_rotate_pair(x[0], x[1], cc[0], ss[0]);
+          rope_rotate_pair(x[2], x[3], cc[1], ss[1]);
+          o = make_float4(x[0], x[1], x[2], x[3]);
+        }
+        reinterpret_cast<Vec*>(static_cast<char*>(which ? k : q))[off * ESZ / 16] = o;
+      }
+    }
+  };
   for (int f0 = tok_begin; f0 < tok_end; f0 += kRunMax) {
     const int nf = min(kRunMax, tok_end - f0);
+    const int n_items = (active && rotated && nf > t_off) ? ((nf - t_off + U * tpi - 1) / (U * tpi)) * nrem : 0;
+    Vec wa[2][U], wb[2][U];
+    // The first item's loads go out before the table is computed.
+    if (n_items > 0) load(f0, nf, 0, wa);
     // cos/sin of the fill's tokens: entry (t, pair) at t * 64 + pair
     for (int e = tid; e < nf * 64; e += 256) {
       const int t = e >> 6, pair = e & 63;
@@ -78,70 +147,14 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
       cs[e] = make_float2(c, sn);
     }
     __syncthreads();
-    if (active && rotated) {
-      constexpr int U = 4;  // tokens in flight per thread
-      for (int tl = t_off; tl < nf; tl += U * tpi) {
-        for (int rem = rem0; rem < V; rem += 256) {
-          const int head = rem / VPR;
-          long long off[U];
-          bool live[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            off[u] = static_cast<long long>(f0 + tl + u * tpi) * p.row_stride + head * 128 + g * (16 / ESZ);
-            live[u] = tl + u * tpi < nf && in_bounds(off[u], 16 / ESZ, p.extent, p.err);
-          }
-          Vec w[2][U];
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            if (which >= nt) break;
-            const Vec* base = reinterpret_cast<const Vec*>(static_cast<const char*>(which ? k : q));
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-              if (live[u]) w[which][u] = base[off[u] * ESZ / 16];
-          }
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            if (!live[u]) continue;
-            const float4* tab = reinterpret_cast<const float4*>(&cs[(tl + u * tpi) * 64 + g * PPV]);
-            float cc[PPV], ss[PPV];
-#pragma unroll
-            for (int h2 = 0; h2 < PPV / 2; ++h2) {
-              const float4 t4 = tab[h2];
-              cc[2 * h2] = t4.x;
-              ss[2 * h2] = t4.y;
-              cc[2 * h2 + 1] = t4.z;
-              ss[2 * h2 + 1] = t4.w;
-            }
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-              if (which >= nt) break;
-              Vec o;
-              if constexpr (kBF16) {
-                const uint32_t* v = reinterpret_cast<const uint32_t*>(&w[which][u]);
-                uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  float x0 = __uint_as_float(v[e] << 16);
-                  float x1 = __uint_as_float(v[e] & 0xFFFF0000u);
-                  rope_rotate_pair(x0, x1, cc[e], ss[e]);
-                  __nv_bfloat162 t2 = __floats2bfloat162_rn(x0, x1);
-                  ov[e] = *reinterpret_cast<const uint32_t*>(&t2);
-                }
-              } else {
-                const float* v = reinterpret_cast<const float*>(&w[which][u]);
-                float x[4] = {v[0], v[1], v[2], v[3]};
-                rope_rotate_pair(x[0], x[1], cc[0], ss[0]);
-                rope_rotate_pair(x[2], x[3], cc[1], ss[1]);
-                o = make_float4(x[0], x[1], x[2], x[3]);
-              }
-              Vec* base = reinterpret_cast<Vec*>(static_cast<char*>(which ? k : q));
-              base[off[u] * ESZ / 16] = o;
-            }
-          }
-        }
-      }
+    // Two buffers: the next item's loads are in flight while this one rotates.
+    for (int i = 0; i < n_items; i += 2) {
+      if (i + 1 < n_items) load(f0, nf, i + 1, wb);
+      rotate_store(f0, nf, i, wa);
+      if (i + 2 < n_items) load(f0, nf, i + 2, wa);
+      if (i + 1 < n_items) rotate_store(f0, nf, i + 1, wb);
     }
-    __syncthreads();
+    __syncthreads();  // the table's readers are done before the next fill rewrites it
   }
 }
 

@@ -44,7 +44,7 @@ namespace nomas {
 namespace attn {
 
 constexpr int kI8HalfBytes = 64 * 128;      // one CTA's half of an int8 tile: [64 rows][128 B], 128B-swizzled
-constexpr int kHalfPanelBytes = 64 * 128;   // 64 rows of one bf16 panel (one CTA's half of it)
+constexpr int kWarpRowBytes = 16 * 128;     // 16 rows of one bf16 panel (one filler warp's share of a half)
 
 template <bool kInt8>
 struct Layout {
@@ -60,8 +60,7 @@ struct Layout {
   static constexpr int bRingEmpty = bRingFull + NS;
   static constexpr int bStageFull = bRingEmpty + NS;
   static constexpr int bStageEmpty = bStageFull + NI;
-  static constexpr int bHalfReady = bStageEmpty + NI;  // [NI] INT8: this CTA's half tile is in its ring
-  static constexpr int bSFull = bHalfReady + NI;   // [2]
+  static constexpr int bSFull = bStageEmpty + NI;  // [2]
   static constexpr int bPFull = bSFull + 2;         // [2]
   static constexpr int bPVDone = bPFull + 2;        // [2]
   static constexpr int bFinal = bPVDone + 2;
@@ -112,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::NI; ++s) {
       mbar_init(&bars[L::bStageFull + s], 1);
       mbar_init(&bars[L::bStageEmpty + s], 4);  // one arrival per filler warp
-      mbar_init(&bars[L::bHalfReady + s], 4);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[L::bSFull + t], 1);
@@ -335,8 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // query blocks) and share every dequantised tile: each CTA dequantises
     // its half (64 rows) of each int8 cache tile, x_hat = bf16(code * scale),
     // into its own ring slot, and the copy engine then moves that half into
-    // the partner's slot (two 8 KB shared-to-shared bulk copies that complete
-    // transactions on the partner's full-barrier).  Current-segment bf16
+    // the partner's slot: each filler warp copies the 16 rows of each panel it
+    // wrote (2 KB shared-to-shared bulk copies that complete transactions on
+    // the partner's full-barrier) as soon as it wrote them.  Current-segment bf16
     // tiles are fetched by TMA into the local ring (issued by warp 12).  Each
     // local filler warp arrives once on a slot's full-barrier (count 4), and a
     // slot is reused only after both CTAs' MMA warps released it, so neither
@@ -439,27 +438,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&bars[L::bHalfReady + si]);
-            if (warp == 12) {
-              // The partner's half arrives as 16 KB of transactions on this slot.
-              mbar_expect_tx(fb, 2 * kHalfPanelBytes);
-              // Once all four local warps wrote this CTA's half, copy it (64 rows
-              // of each 128-row panel, contiguous) into the partner's slot.
-              if (!lane_wait(&bars[L::bHalfReady + si], ui & 1, ab, p.err)) {
-                ok = false;
-              } else {
-                const uint32_t peer_fb = mapa_shared(smem_u32(fb), peer);
-                for (int pn = 0; pn < 2; ++pn) {
-                  const uint8_t* half_src = sRing + s * kTileBytes + pn * kPanelBytes + 64 * rank * 128;
-                  bulk_copy_to_cluster(mapa_shared(smem_u32(half_src), peer), half_src, kHalfPanelBytes,
-                                       peer_fb);
-                }
-              }
+            // This warp wrote rows 16 (warp - 12) .. + 15 of this CTA's half in
+            // both panels (2 KB each, contiguous): copy them into the partner's
+            // slot at once, and expect the partner's matching 4 KB here.  Each
+            // warp raises the expected bytes before its own arrival, so the
+            // phase cannot complete before all 16 KB of the partner's half land.
+            mbar_expect_tx(fb, 2 * kWarpRowBytes);
+            const uint32_t peer_fb = mapa_shared(smem_u32(fb), peer);
+            for (int pn = 0; pn < 2; ++pn) {
+              const uint8_t* rows_src =
+                  sRing + s * kTileBytes + pn * kPanelBytes + (64 * rank + 16 * (warp - 12)) * 128;
+              bulk_copy_to_cluster(mapa_shared(smem_u32(rows_src), peer), rows_src, kWarpRowBytes, peer_fb);
             }
             mbar_arrive(fb);
             mbar_arrive(&bars[L::bStageEmpty + si]);
           }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           ++ri;
         }
       }

@@ -17,8 +17,8 @@
 // the cache, so callers may keep them across the denoising steps of a turn.
 // select_kernel, one CTA per (query group, head), reads the group's queries
 // (a 256-byte row slice per query, eight loads in flight per thread), scores
-// every tile, ranks the scores and writes the kept list with a block-wide
-// prefix count.
+// every tile, selects the k best by a radix selection on the scores' bits
+// and writes the kept list in tile order with block-wide prefix counts.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -109,8 +109,7 @@ constexpr int kPickThreads = 512;
 
 __global__ void __launch_bounds__(kPickThreads, 2) select_kernel(const SparseSelectParams p) {
   // Dynamic shared memory: first the partial query sums [32][129], later
-  // (after a barrier) the scores [n4 * 4] (padded with -inf) followed by keep
-  // flags [n_tiles].
+  // (after a barrier) the scores [n_tiles], turned into selection keys in place.
   extern __shared__ float s_dyn[];
   float(*part)[129] = reinterpret_cast<float(*)[129]>(s_dyn);
   float* s_scores = s_dyn;
@@ -183,44 +182,89 @@ __global__ void __launch_bounds__(kPickThreads, 2) select_kernel(const SparseSel
     a += __shfl_xor_sync(0xffffffffu, a, 2);
     if (t < p.n_tiles && qd == 0) s_scores[t] = a;
   }
-  const int n4 = (p.n_tiles + 3) >> 2;
-  if (threadIdx.x < 4 * n4 - p.n_tiles) s_scores[p.n_tiles + threadIdx.x] = -INFINITY;
   __syncthreads();
 
-  // Rank = tiles with a higher score, or an equal score and a lower index:
-  // tiles before t count when su >= st, tiles after t when su > st (the -inf
-  // padding never counts).  Four scores per shared-memory load.
-  unsigned char* keep = reinterpret_cast<unsigned char*>(s_scores + 4 * n4);
-  const float4* s4 = reinterpret_cast<const float4*>(s_scores);
+  // Top-k by radix selection.  Scores become order-preserving 32-bit keys
+  // (-0 folded into +0 first, so equal scores give equal keys); four 8-bit
+  // passes, most significant first, histogram the keys that match the prefix
+  // found so far and pick the digit where the count of larger keys reaches
+  // k.  That leaves the k-th largest key K and how many tiles equal to K are
+  // kept (`need`): every key > K, and the first `need` keys == K in tile
+  // order (ties to the lower tile).  Linear in the tile count.
+  uint32_t* s_keys = reinterpret_cast<uint32_t*>(s_scores);
   for (int t = threadIdx.x; t < p.n_tiles; t += kPickThreads) {
-    const float st = s_scores[t];
-    const int tc = t >> 2;
-    int rank = 0;
-    for (int u4 = 0; u4 < tc; ++u4) {
-      const float4 v = s4[u4];
-      rank += (v.x >= st) + (v.y >= st) + (v.z >= st) + (v.w >= st);
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int u = 4 * tc + e;
-      const float su = s_scores[u];
-      rank += u < t ? (su >= st) : (u > t ? (su > st) : 0);
-    }
-    for (int u4 = tc + 1; u4 < n4; ++u4) {
-      const float4 v = s4[u4];
-      rank += (v.x > st) + (v.y > st) + (v.z > st) + (v.w > st);
-    }
-    keep[t] = rank < p.keep ? 1 : 0;
+    const uint32_t u = __float_as_uint(s_scores[t] + 0.0f);
+    s_keys[t] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   }
-  __syncthreads();
+  __shared__ uint32_t s_hist[256];
+  __shared__ uint32_t s_sel[2];  // prefix of K found so far, tiles still to take among the matching ones
+  uint32_t prefix = 0u, mask = 0u;
+  int need = p.keep;
+  const bool keep_all = p.keep >= p.n_tiles;
+  if (!keep_all) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (threadIdx.x < 256) s_hist[threadIdx.x] = 0u;
+      __syncthreads();
+      for (int t = threadIdx.x; t < p.n_tiles; t += kPickThreads) {
+        const uint32_t key = s_keys[t];
+        if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // Lane l holds digits 255 - 8 l .. 248 - 8 l (descending).
+        uint32_t c[8], lane_sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = s_hist[255 - 8 * lane - i];
+          lane_sum += c[i];
+        }
+        uint32_t incl = lane_sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        uint32_t above = incl - lane_sum;  // matching keys with a larger digit than this lane's
+        if (above < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= incl) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (above + c[i] >= static_cast<uint32_t>(need)) {
+              s_sel[0] = prefix | (static_cast<uint32_t>(255 - 8 * lane - i) << shift);
+              s_sel[1] = static_cast<uint32_t>(need) - above;
+              break;
+            }
+            above += c[i];
+          }
+        }
+      }
+      __syncthreads();
+      prefix = s_sel[0];
+      need = static_cast<int>(s_sel[1]);
+      mask |= 255u << shift;
+    }
+  }
 
-  // Kept tiles in increasing order: position = kept tiles before this one.
+  // Kept tiles in increasing order: a tile is kept if its key exceeds K, or
+  // equals K and fewer than `need` tiles equal to K come before it; its
+  // position is the number of kept tiles before it (two block-wide prefix
+  // counts per pass of 512 tiles).
   const size_t hg = static_cast<size_t>(h) * p.n_groups + g;
   int* out = p.tiles + hg * p.max_keep;
-  int base = 0;
+  int base = 0, base_eq = 0;
   for (int t0 = 0; t0 < p.n_tiles; t0 += kPickThreads) {
     const int t = t0 + threadIdx.x;
-    const bool k = t < p.n_tiles && keep[t];
+    const bool live = t < p.n_tiles;
+    const uint32_t key = live ? s_keys[t] : 0u;
+    const bool eq = live && !keep_all && key == prefix;
+    const unsigned bal_eq = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) s_warp[warp] = __popc(bal_eq);
+    __syncthreads();
+    int eq_before = base_eq;
+    for (int w = 0; w < warp; ++w) eq_before += s_warp[w];
+    eq_before += __popc(bal_eq & ((1u << lane) - 1u));
+    for (int w = 0; w < kPickThreads / 32; ++w) base_eq += s_warp[w];
+    __syncthreads();
+    const bool k = live && (keep_all || key > prefix || (eq && eq_before < need));
     const unsigned bal = __ballot_sync(0xffffffffu, k);
     if (lane == 0) s_warp[warp] = __popc(bal);
     __syncthreads();
@@ -239,7 +283,7 @@ __global__ void __launch_bounds__(kPickThreads, 2) select_kernel(const SparseSel
 }  // namespace
 
 size_t sparse_select_smem(int n_tiles) {
-  const size_t need = static_cast<size_t>((n_tiles + 3) & ~3) * 4 + n_tiles, part = 32 * 129 * sizeof(float);
+  const size_t need = static_cast<size_t>(n_tiles) * 4, part = 32 * 129 * sizeof(float);
   return ((need > part ? need : part) + 15) & ~size_t(15);
 }
 

@@ -279,3 +279,17 @@ def test_bench_flop_accounting_is_consistent():
     s5 = CONFIGS["c5_session12"]
     assert bench.session_flops(s5, 12, keep=1.0) == bench.session_flops(s5, 12)
     assert bench.session_flops(s5, 12, keep=0.25) < bench.session_flops(s5, 12)
+
+
+def test_bench_traffic_provenance_reads_for_every_config():
+    # bench.py takes roofline.traffic from the committed ncu summary only while
+    # the attention sources hash the same; every config must get an answer
+    # (a number, or None with the reason), never an error.
+    import bench
+    from synth import CONFIG_ORDER
+    for name in CONFIG_ORDER:
+        traffic, source = bench._load_traffic(name)
+        assert traffic is None or traffic > 0
+        assert isinstance(source, str) and source
+    for rel in bench.ATTN_SOURCES:
+        assert os.path.exists(os.path.join(ROOT, rel)), rel

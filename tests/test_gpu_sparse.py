@@ -127,6 +127,36 @@ def test_select_planted_tile_always_kept_and_empty_cache():
     assert torch.all(tiles[..., 0] == 5)
 
 
+@pytest.mark.parametrize("cache_dtype", ["bf16", "int8"])
+def test_select_exact_ties_go_to_the_lower_tile(cache_dtype):
+    # Eight resident tiles (one 8 x 16 frame each) whose keys are identical
+    # except that tiles 2 and 6 are scaled up: their mean keys, and so their
+    # scores, are exactly equal within each group of equal tiles.  Keeping 4
+    # of 8 takes tiles 2 and 6 (the larger scores, given a positive mean query)
+    # and then the two lowest of the tied rest, 0 and 1.
+    from synth import segment_kv
+    wl = small_variant(_variant(1), heads=2, grid_h=8, grid_w=16, cache_frames_hist=(8,), cur_frames=1, n_text=0,
+                       cache_dtype=cache_dtype, past_frames=0, capacity_frames=8)
+    k1, v1 = segment_kv(wl, 0, 1, 0)
+    k = np.concatenate([k1] * 8, axis=0).copy()
+    v = np.concatenate([v1] * 8, axis=0)
+    k += 0.5                                   # positive mean key in every tile
+    k[2 * 128:3 * 128] *= 2.0
+    k[6 * 128:7 * 128] *= 2.0
+    q, _, _ = current_qkv(wl)
+    q = np.abs(q) + 0.1                        # positive mean query: larger keys score higher
+    gc = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, 8, 0, cache_dtype)
+    gc.append(to_dev(k, "bf16"), to_dev(v, "bf16"))
+    tiles, counts = nomas.sparse_select(gc, 0, to_dev(q, "bf16"), wl.n_video, wl.n_text, 0.5)
+    torch.cuda.synchronize()
+    assert torch.all(counts == 4)
+    for h in range(wl.heads):
+        assert tiles[h, 0, :4].tolist() == [0, 1, 2, 6]
+    # keep one of eight: the lower of the two largest
+    tiles, counts = nomas.sparse_select(gc, 0, to_dev(q, "bf16"), wl.n_video, wl.n_text, 0.125)
+    assert torch.all(counts == 1) and torch.all(tiles[..., 0] == 2)
+
+
 def _oracle_inputs(wl, oc, q, k):
     qr = o_rope.rope3d_segment(q, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
     kr = o_rope.rope3d_segment(k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
