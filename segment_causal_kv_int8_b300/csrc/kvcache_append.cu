@@ -158,15 +158,16 @@ __device__ __forceinline__ void store_row16(const AppendParams& p, int tensor, l
       // rint(fl32(x * inv)) in [-127, 127]: adding 1.5 * 2^23 rounds to an
       // integer (ties to even) whose low byte is the two's-complement code.
       // The product is rounded on its own (the packed multiply) and the add
-      // is a separate scalar __fadd_rn, so nothing fuses the two into an FMA.
+      // is a separate packed add, so nothing fuses the two into an FMA.
       const uint64_t inv2 = f2_pack(inv, inv);
+      const uint64_t magic2 = f2_pack(12582912.0f, 12582912.0f);
       uint32_t bb[16];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         float y0, y1;
-        f2_unpack(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), y0, y1);
-        bb[2 * e] = __float_as_uint(__fadd_rn(y0, 12582912.0f));
-        bb[2 * e + 1] = __float_as_uint(__fadd_rn(y1, 12582912.0f));
+        f2_unpack(f2_add(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), magic2), y0, y1);
+        bb[2 * e] = __float_as_uint(y0);
+        bb[2 * e + 1] = __float_as_uint(y1);
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -251,27 +252,29 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
 
 // Direct append for bf16 input: 8 lanes own a row (16 values each, two
 // 16-byte loads), so the per-row reduction and the two divisions are shared by
-// twice as many values.  Grid: x = groups of kAppendTokens tokens, y = groups
-// of 32 heads, z = (block, tensor); a CTA's 32 row groups are consecutive
-// heads.  A BF16 cache takes the bf16 values unchanged (a copy).
+// twice as many values.  A CTA takes 64 consecutive (token, head) rows of the
+// input, one contiguous 16 KB range, two rows per 8-lane group (both loads of
+// both rows issued first).  Grid: x = groups of 64 rows, z = (block, tensor).
+// A BF16 cache takes the bf16 values unchanged (a copy).
+constexpr int kAppend8Rows = 64;
+
 template <int K>
-__global__ void __launch_bounds__(256, K != kCacheBF16 ? 6 : 8) append8_kernel(const __grid_constant__ AppendParams p) {
-  const int h = blockIdx.y * 32 + (threadIdx.x >> 3);
-  if (h >= p.heads) return;  // whole 8-lane groups leave together
+__global__ void __launch_bounds__(256, K != kCacheBF16 ? 5 : 8) append8_kernel(const __grid_constant__ AppendParams p) {
   const int g = threadIdx.x & 7;
   const unsigned gmask = 0xFFu << (threadIdx.x & 24);
   const int tensor = blockIdx.z & 1;
   const int b = blockIdx.z >> 1;
-  const int n0 = blockIdx.x * kAppendTokens;
+  // rows = n_tokens * heads < 2^31 (checked by the launcher)
+  const int rows = p.n_tokens * p.heads;
+  const int r0 = static_cast<int>(blockIdx.x) * kAppend8Rows;
+  const long long src0 = b * p.block_stride + static_cast<long long>(p.first_frame) * p.tpf * p.heads * 128;
   const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(tensor ? p.v : p.k);
-  const long long plane = static_cast<long long>(b) * p.heads + h;
-  uint4 w[kAppendTokens][2];
+  uint4 w[2][2];
 #pragma unroll
-  for (int r = 0; r < kAppendTokens; ++r) {
-    const int n = n0 + r;
-    if (n < p.n_tokens) {
-      const long long src_tok = static_cast<long long>(p.first_frame) * p.tpf + n;
-      const long long off = b * p.block_stride + (src_tok * p.heads + h) * 128 + 16 * g;
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + (threadIdx.x >> 3) + 32 * r;
+    if (row < rows) {
+      const long long off = src0 + static_cast<long long>(row) * 128 + 16 * g;
       if (in_bounds(off, 16, p.src_extent, p.err)) {
         const uint4* q = reinterpret_cast<const uint4*>(src + off);
         w[r][0] = q[0];
@@ -282,13 +285,16 @@ __global__ void __launch_bounds__(256, K != kCacheBF16 ? 6 : 8) append8_kernel(c
     }
   }
 #pragma unroll
-  for (int r = 0; r < kAppendTokens; ++r) {
-    const int n = n0 + r;
-    if (n >= p.n_tokens) break;
-    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + (threadIdx.x >> 3) + 32 * r;
+    if (row >= rows) break;  // rows of one 8-lane group: uniform
+    const int n = static_cast<int>(static_cast<unsigned>(row) / static_cast<unsigned>(p.heads));
+    const int h = row - n * p.heads;
+    const int f = static_cast<int>(static_cast<unsigned>(n) / static_cast<unsigned>(p.tpf));  // one wrap at most
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
-    const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
+    const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
+                              static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
     if constexpr (K != kCacheBF16) {
       const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
       float x[16];
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(256, K != kCacheBF16 ? 6 : 8) append8_kernel(c
         x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
       }
       store_row16<K>(p, tensor, dst_row, x, g, gmask);
-    } else {
+    } else if (in_bounds(dst_row, 1, p.cache_rows, p.err)) {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(tensor ? p.cv : p.ck) + dst_row * 128 + 16 * g);
       dst[0] = w[r][0];
       dst[1] = w[r][1];
@@ -644,9 +650,10 @@ cudaError_t launch_staged(const AppendParams& p, unsigned grid, cudaStream_t str
 template <int K>
 cudaError_t launch_direct(bool f32_in, const AppendParams& p, cudaStream_t stream) {
   if (!f32_in) {
-    const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
-                    static_cast<unsigned>((p.heads + 31) / 32), static_cast<unsigned>(2 * p.blocks));
-    if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
+    const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
+    const long long cta = (rows + kAppend8Rows - 1) / kAppend8Rows;
+    if (rows >= 0x7FFFFFFFLL - kAppend8Rows || 2LL * p.blocks > 65535) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(cta), 1, static_cast<unsigned>(2 * p.blocks));
     append8_kernel<K><<<grid, 256, 0, stream>>>(p);
   } else {
     const dim3 grid(static_cast<unsigned>((p.n_tokens + kAppendTokens - 1) / kAppendTokens),
