@@ -145,17 +145,9 @@ def rope_bytes(wl) -> int:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_sample(wl, seconds: float, block: int = 0):
-    """Time the oracle's RoPE + segment attention on a sample of query rows.
-
-    Returns (flops_per_second, description, threads, seconds).  The sample
-    grows until it takes at least ``seconds`` (capped at the whole segment).
-    """
-    import numpy as np
-
-    from oracle import attention as o_attn
+def oracle_setup(wl, block: int = 0):
+    """The oracle's inputs for one block call of ``wl`` (cache built by the oracle's own append)."""
     from oracle import ring_cache as o_cache
-    from oracle import rope3d as o_rope
     from synth import current_qkv, history_segments
 
     oc = o_cache.RingCache(1, wl.heads, wl.head_dim, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames,
@@ -164,8 +156,23 @@ def oracle_sample(wl, seconds: float, block: int = 0):
         oc.append(k[None], v[None])
     q, k, v = current_qkv(wl, block=block)
     kc, vc = oc.cache_kv(0)
+    return q, k, v, kc, vc
+
+
+def oracle_sample(wl, seconds: float, block: int = 0, inputs=None, rows: int = 64):
+    """Time the oracle's RoPE + segment attention on a sample of query rows.
+
+    Returns (flops_per_second, description, threads, seconds, rows).  The
+    sample grows from ``rows`` until it takes at least ``seconds`` (capped at
+    the whole segment).  ``inputs``: a reused ``oracle_setup`` result.
+    """
+    import numpy as np
+
+    from oracle import attention as o_attn
+    from oracle import rope3d as o_rope
+
+    q, k, v, kc, vc = inputs if inputs is not None else oracle_setup(wl, block)
     scale = o_attn.default_scale(wl.head_dim)
-    rows = 64
     while True:
         sel = np.linspace(0, wl.n_q - 1, rows).astype(np.int64)
         t0 = time.perf_counter()
@@ -180,7 +187,7 @@ def oracle_sample(wl, seconds: float, block: int = 0):
     threads = _blas_threads()
     desc = (f"oracle RoPE + segment attention (float64 numpy) on {rows} of {wl.n_q} query rows x all "
             f"{wl.heads} heads x {wl.n_k} keys of {wl.name}; {dt:.1f} s")
-    return flops / dt, desc, threads, dt
+    return flops / dt, desc, threads, dt, rows
 
 
 def _blas_threads():
@@ -202,11 +209,13 @@ def run_reference(args):
 
     wl = CONFIGS[args.config]
     per_step = max(2.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    inputs = oracle_setup(wl)  # built once; every step times RoPE + attention on a sample of rows
+    rows = 64
     for _ in range(args.warmup):
-        oracle_sample(wl, per_step)
+        _, _, _, _, rows = oracle_sample(wl, per_step, inputs=inputs, rows=rows)
     vals, times = [], []
     for _ in range(args.steps):
-        v, desc, threads, dt = oracle_sample(wl, per_step)
+        v, desc, threads, dt, rows = oracle_sample(wl, per_step, inputs=inputs, rows=rows)
         vals.append(v)
         times.append(dt)
     value = statistics.median(vals) / 1e12
@@ -673,7 +682,7 @@ def run_ours(args):
                                                                          total_ms)}
             line["roofline"]["kernel"] += " (tile lists)"
         if not args.no_cpu_baseline and world == 1:
-            v_cpu, desc, threads, _ = oracle_sample(wl, args.cpu_seconds)
+            v_cpu, desc, threads, _, _ = oracle_sample(wl, args.cpu_seconds)
             line["cpu_baseline"] = {"value": v_cpu / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                                     "sample": desc}
         print(json.dumps(line), flush=True)

@@ -20,13 +20,15 @@
 // tokens), whose loads are all issued before any arithmetic.  Scores are
 // reduced over the 16 lanes with four shuffles, the four rows' reductions
 // interleaved; the softmax over the n_cam scores runs online in float32 (log2
-// domain).
+// domain, ex2.approx), with packed f32x2 arithmetic for the dot products and
+// the output update.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "checks.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace nomas {
 namespace {
@@ -99,9 +101,13 @@ __global__ void __launch_bounds__(256) camera_attn_kernel(const __grid_constant_
     float sc[kCamRowsPerGroup];
 #pragma unroll
     for (int r = 0; r < kCamRowsPerGroup; ++r) {
-      sc[r] = 0.0f;
+      // two interleaved partial sums in one packed f32x2 accumulator
+      uint64_t acc = f2_mul(f2_pack(q[r][0], q[r][1]), f2_pack(k[0], k[1]));
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sc[r] = fmaf(q[r][e], k[e], sc[r]);
+      for (int e = 2; e < 8; e += 2) acc = f2_fma(f2_pack(q[r][e], q[r][e + 1]), f2_pack(k[e], k[e + 1]), acc);
+      float a0, a1;
+      f2_unpack(acc, a0, a1);
+      sc[r] = a0 + a1;
     }
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1)
@@ -111,11 +117,15 @@ __global__ void __launch_bounds__(256) camera_attn_kernel(const __grid_constant_
     for (int r = 0; r < kCamRowsPerGroup; ++r) {
       const float s = sc[r] * p.scale_log2;
       const float m_new = fmaxf(m[r], s);
-      const float alpha = exp2f(m[r] - m_new);
-      const float pj = exp2f(s - m_new);
+      const float alpha = fast_exp2(m[r] - m_new);  // 0 on the first camera token (m = -inf)
+      const float pj = fast_exp2(s - m_new);
       l[r] = fmaf(l[r], alpha, pj);
+      const uint64_t a2 = f2_pack(alpha, alpha), p2 = f2_pack(pj, pj);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[r][e] = fmaf(o[r][e], alpha, pj * v[e]);
+      for (int e = 0; e < 8; e += 2) {
+        const uint64_t o2 = f2_fma(f2_pack(o[r][e], o[r][e + 1]), a2, f2_mul(p2, f2_pack(v[e], v[e + 1])));
+        f2_unpack(o2, o[r][e], o[r][e + 1]);
+      }
       m[r] = m_new;
     }
   }

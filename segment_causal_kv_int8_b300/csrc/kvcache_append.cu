@@ -158,16 +158,17 @@ __device__ __forceinline__ void store_row16(const AppendParams& p, int tensor, l
       // rint(fl32(x * inv)) in [-127, 127]: adding 1.5 * 2^23 rounds to an
       // integer (ties to even) whose low byte is the two's-complement code.
       // The product is rounded on its own (the packed multiply) and the add
-      // is a separate packed add, so nothing fuses the two into an FMA.
+      // is a separate scalar __fadd_rn: a packed add right after the packed
+      // multiply is contracted into a fused multiply-add, which skips the
+      // product's rounding and can move a tie to the other code.
       const uint64_t inv2 = f2_pack(inv, inv);
-      const uint64_t magic2 = f2_pack(12582912.0f, 12582912.0f);
       uint32_t bb[16];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         float y0, y1;
-        f2_unpack(f2_add(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), magic2), y0, y1);
-        bb[2 * e] = __float_as_uint(y0);
-        bb[2 * e + 1] = __float_as_uint(y1);
+        f2_unpack(f2_mul(f2_pack(x[2 * e], x[2 * e + 1]), inv2), y0, y1);
+        bb[2 * e] = __float_as_uint(__fadd_rn(y0, 12582912.0f));
+        bb[2 * e + 1] = __float_as_uint(__fadd_rn(y1, 12582912.0f));
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)

@@ -158,22 +158,193 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
   }
 }
 
+// ---------------------------------------------------------------- async-copy form
+// Each CTA takes an equal run of tokens and streams it in items of T tokens
+// (T * heads * 16 vectors of each of Q and K, at most 4 vectors per thread per
+// tensor).  Every thread fetches its own vectors of an item with 16-byte
+// cp.async copies into a 3-stage shared-memory ring, so up to 3 items (24
+// copies, 384 bytes per thread) are in flight without holding registers, and
+// reads them back itself once its copy group has landed (no barrier): rotate,
+// then store to global memory.  The item layout is the same for every item,
+// so a thread's (token, head, pair group) of each vector is computed once.
+constexpr int kAsyncStages = 3;
+constexpr int kAsyncVecs = 1024;  // vectors per tensor per item (16 KB)
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q, void* __restrict__ k,
+                                                           const __grid_constant__ RopeParams p, TwoPi tp,
+                                                           int run_tokens, int item_tokens) {
+  constexpr int VPR = kBF16 ? 16 : 32;  // vectors per head row
+  constexpr int PPV = kBF16 ? 4 : 2;    // rotary pairs per vector
+  constexpr int ESZ = kBF16 ? 2 : 4;
+  constexpr int M = kAsyncVecs / 256;   // vectors per thread per tensor per item
+  using Vec = typename std::conditional<kBF16, uint4, float4>::type;
+  extern __shared__ __align__(16) uint8_t asm_raw[];
+  Vec* ring = reinterpret_cast<Vec*>(asm_raw);                                       // [stage][tensor][kAsyncVecs]
+  float2* cs = reinterpret_cast<float2*>(asm_raw + kAsyncStages * 2 * kAsyncVecs * 16);  // [kRunMax][64]
+  __shared__ int8_t axis_s[64];
+  const int tid = threadIdx.x;
+  if (tid < 64) axis_s[tid] = p.axis[tid];
+  const int tok_begin = blockIdx.x * run_tokens;
+  const int tok_end = min(p.n_video, tok_begin + run_tokens);
+  const int V = p.heads * VPR;
+  const int T = item_tokens;                 // T * V <= kAsyncVecs
+  const int g = tid & (VPR - 1);             // the thread's pair group (fixed: 256 % VPR == 0)
+  int tl_m[M], hoff_m[M];                    // token within the item, element offset within the token row
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int j = tid + 256 * m;
+    tl_m[m] = j < T * V ? j / V : T;         // T: this slot is unused
+    hoff_m[m] = ((j - (j / V) * V) / VPR) * 128 + g * (16 / ESZ);
+  }
+  __syncthreads();
+  bool rotated = false;
+#pragma unroll
+  for (int e = 0; e < PPV; ++e) rotated |= axis_s[g * PPV + e] >= 0;
+  const int nt = (k != nullptr) ? 2 : 1;
+  for (int f0 = tok_begin; f0 < tok_end; f0 += kRunMax) {
+    const int nf = min(kRunMax, tok_end - f0);
+    const int n_items = (nf + T - 1) / T;
+    auto fetch = [&](int i) {
+      if (rotated && i < n_items) {
+        Vec* st = ring + (i % kAsyncStages) * 2 * kAsyncVecs;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const int tl = i * T + tl_m[m];
+          if (tl_m[m] >= T || tl >= nf) continue;
+          const long long off = static_cast<long long>(f0 + tl) * p.row_stride + hoff_m[m];
+          if (!in_bounds(off, 16 / ESZ, p.extent, p.err)) continue;
+          for (int w = 0; w < nt; ++w)
+            cp_async16(&st[w * kAsyncVecs + tid + 256 * m], static_cast<const char*>(w ? k : q) + off * ESZ);
+        }
+      }
+      cp_async_commit();  // one group per item, empty or not, so the group count stays uniform
+    };
+    for (int i = 0; i < kAsyncStages - 1; ++i) fetch(i);
+    // cos/sin of the fill's tokens while the first items are in flight
+    for (int e = tid; e < nf * 64; e += 256) {
+      const int t = e >> 6, pair = e & 63;
+      const int a = axis_s[pair];
+      float c = 1.0f, sn = 0.0f;
+      if (a >= 0) {
+        const int tok = f0 + t;
+        const int frame = tok / p.tpf;
+        const int within = tok - frame * p.tpf;
+        const int row = within / p.grid_w;
+        const float pos = a == 0 ? static_cast<float>(p.t0 + frame)
+                                 : static_cast<float>(a == 1 ? row : within - row * p.grid_w);
+        sincosf(rope_reduced_angle(pos, p.f_hi[pair], p.f_lo[pair], tp), &sn, &c);
+      }
+      cs[e] = make_float2(c, sn);
+    }
+    __syncthreads();
+    for (int i = 0; i < n_items; ++i) {
+      fetch(i + kAsyncStages - 1);
+      cp_async_wait<kAsyncStages - 1>();  // this thread's copies of item i have landed
+      if (!rotated) continue;
+      const Vec* st = ring + (i % kAsyncStages) * 2 * kAsyncVecs;
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int tl = i * T + tl_m[m];
+        if (tl_m[m] >= T || tl >= nf) continue;
+        const long long off = static_cast<long long>(f0 + tl) * p.row_stride + hoff_m[m];
+        if (!in_bounds(off, 16 / ESZ, p.extent, p.err)) continue;
+        const float4* tab = reinterpret_cast<const float4*>(&cs[tl * 64 + g * PPV]);
+        float cc[PPV], ss[PPV];
+#pragma unroll
+        for (int h2 = 0; h2 < PPV / 2; ++h2) {
+          const float4 t4 = tab[h2];
+          cc[2 * h2] = t4.x;
+          ss[2 * h2] = t4.y;
+          cc[2 * h2 + 1] = t4.z;
+          ss[2 * h2 + 1] = t4.w;
+        }
+        for (int w = 0; w < nt; ++w) {
+          Vec v = st[w * kAsyncVecs + tid + 256 * m];
+          if constexpr (kBF16) {
+            uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float x0 = __uint_as_float(u[e] << 16);
+              float x1 = __uint_as_float(u[e] & 0xFFFF0000u);
+              rope_rotate_pair(x0, x1, cc[e], ss[e]);
+              __nv_bfloat162 t2 = __floats2bfloat162_rn(x0, x1);
+              u[e] = *reinterpret_cast<const uint32_t*>(&t2);
+            }
+          } else {
+            rope_rotate_pair(v.x, v.y, cc[0], ss[0]);
+            rope_rotate_pair(v.z, v.w, cc[1], ss[1]);
+          }
+          reinterpret_cast<Vec*>(static_cast<char*>(w ? k : q))[off * ESZ / 16] = v;
+        }
+      }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // the table's readers are done before the next fill rewrites it
+  }
+}
+
+constexpr int kAsyncSmem = kAsyncStages * 2 * kAsyncVecs * 16 + kRunMax * 64 * 8;
+
 }  // namespace
 
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream) {
   if (p.n_video <= 0) return cudaSuccess;
   const TwoPi tp = rope_two_pi();
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = 148;
+  const int V = p.heads * (bf16_io ? 16 : 32);  // 16-byte vectors per token row
+  if (V <= kAsyncVecs && dev >= 0 && dev < 64) {
+    // Async-copy form: one resident wave of CTAs (two per SM) with equal runs.
+    static int configured[2][64] = {{0}};
+    if (!configured[bf16_io][dev]) {
+      const cudaError_t e =
+          bf16_io ? cudaFuncSetAttribute(rope3d_async_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kAsyncSmem)
+                  : cudaFuncSetAttribute(rope3d_async_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kAsyncSmem);
+      if (e != cudaSuccess) return e;
+      configured[bf16_io][dev] = 1;
+    }
+    int per_sm = 0;
+    const cudaError_t e =
+        bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_async_kernel<true>, 256, kAsyncSmem)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_async_kernel<false>, 256, kAsyncSmem);
+    if (e != cudaSuccess || per_sm <= 0) {
+      (void)cudaGetLastError();
+      per_sm = 1;
+    }
+    const long long slots = static_cast<long long>(sms) * per_sm;
+    const int run = static_cast<int>((p.n_video + slots - 1) / slots);
+    const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);
+    const int item = kAsyncVecs / V;
+    if (bf16_io)
+      rope3d_async_kernel<true><<<grid, 256, kAsyncSmem, stream>>>(q, k, p, tp, run, item);
+    else
+      rope3d_async_kernel<false><<<grid, 256, kAsyncSmem, stream>>>(q, k, p, tp, run, item);
+    return cudaGetLastError();
+  }
+  // Rows wider than one item: the register-streaming form.
+  int per_sm = 0;
   const cudaError_t e = bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<true>, 256, 0)
                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<false>, 256, 0);
   if (e != cudaSuccess || per_sm <= 0) {
     (void)cudaGetLastError();
-    per_sm = 4;
+    per_sm = 3;
   }
-  // One resident wave of CTAs with equal token runs.
   const long long slots = static_cast<long long>(sms) * per_sm;
   const int run = static_cast<int>((p.n_video + slots - 1) / slots);
   const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(uint32_t* err, uint64_
 // store.  (Launched only in the checked build; the array has a fifth element
 // so the store would stay in bounds even without the check.)
 __global__ void __launch_bounds__(32) bounds_check_kernel(uint32_t* err) {
-  __shared__ uint32_t buf[5];
+  __shared__ volatile uint32_t buf[5];
   if (threadIdx.x == 0 && in_bounds(4, 1, 4, err)) buf[4] = 1u;
 }
 
