@@ -17,6 +17,26 @@ constexpr int kCacheFp8 = 2;
 
 constexpr int kRopeMaxPairs = 64;  // head_dim 128 -> 64 rotary pairs
 
+// Division by a run-time constant d >= 1 as one multiply and one shift
+// (division by invariant integers, Granlund and Montgomery, PLDI 1994): with
+// 2^L >= d > 2^(L-1) and mul = ceil(2^(31+L) / d), which fits 32 bits,
+// (n * mul) >> (31 + L) == n / d for every 0 <= n < 2^31.
+struct FastDiv {
+  uint32_t mul;
+  uint32_t shift;
+};
+inline FastDiv make_fast_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  const uint64_t two = uint64_t(1) << (31 + l);
+  return FastDiv{static_cast<uint32_t>((two + d - 1) / d), 31 + l};
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+  return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(n)) * f.mul) >> f.shift);
+}
+#endif
+
 struct RopeParams {
   float f_hi[kRopeMaxPairs];     // frequency of each pair, high float
   float f_lo[kRopeMaxPairs];     // fl32(f - f_hi): low float of a two-float frequency
@@ -54,6 +74,8 @@ struct AppendParams {
   uint32_t* err;                 // device error word (staged kernel's bounded waits; checked build)
   long long src_extent;          // elements of each input tensor (checked build)
   long long cache_rows;          // blocks * heads * cap_slots rows of each cache tensor (checked build)
+  FastDiv heads_div;             // n / heads
+  FastDiv tpf_div;               // n / tpf
 };
 
 cudaError_t launch_append(bool f32_in, int kind, const AppendParams& p, int sms, cudaStream_t stream);

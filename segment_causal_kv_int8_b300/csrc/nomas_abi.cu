@@ -371,6 +371,8 @@ nomas_status append_impl(nomas_kvcache* cache, const void* k, const void* v, nom
     p.err = nullptr;
     p.src_extent = static_cast<long long>(cache->num_blocks - 1) * block_stride_elems + seg_elems;
     p.cache_rows = static_cast<long long>(cache->num_blocks) * cache->heads * p.cap_slots;
+    p.heads_div = make_fast_div(static_cast<uint32_t>(p.heads));
+    p.tpf_div = make_fast_div(static_cast<uint32_t>(p.tpf));
     int sms = 0;
     if (device_state(&p.err, &sms) != NOMAS_OK) {
       p.err = nullptr;

@@ -166,14 +166,14 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
 // copies, 384 bytes per thread) are in flight without holding registers, and
 // reads them back itself once its copy group has landed (no barrier): rotate,
 // then store to global memory.  The item layout is the same for every item,
-// so a thread's (token, head, pair group) of each vector is computed once.
+// so a thread's (token, head, pair group) of each vector, and its byte offset
+// within an item, are computed once; an item adds one 32-bit offset.  Q and K
+// are separate template cases, so no pointer is chosen at run time.
 constexpr int kAsyncStages = 3;
 constexpr int kAsyncVecs = 1024;  // vectors per tensor per item (16 KB)
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gsrc)
-               : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -181,8 +181,27 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <bool kBF16>
-__global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q, void* __restrict__ k,
+// Rotates the pairs of one 16-byte vector by the (cos, sin) in cc/ss.
+template <bool kBF16, typename Vec>
+__device__ __forceinline__ void rotate_vec(Vec& v, const float (&cc)[kBF16 ? 4 : 2], const float (&ss)[kBF16 ? 4 : 2]) {
+  if constexpr (kBF16) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float x0 = __uint_as_float(u[e] << 16);
+      float x1 = __uint_as_float(u[e] & 0xFFFF0000u);
+      rope_rotate_pair(x0, x1, cc[e], ss[e]);
+      __nv_bfloat162 t2 = __floats2bfloat162_rn(x0, x1);
+      u[e] = *reinterpret_cast<const uint32_t*>(&t2);
+    }
+  } else {
+    rope_rotate_pair(v.x, v.y, cc[0], ss[0]);
+    rope_rotate_pair(v.z, v.w, cc[1], ss[1]);
+  }
+}
+
+template <bool kBF16, bool kTwo>
+__global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q, char* __restrict__ k,
                                                            const __grid_constant__ RopeParams p, TwoPi tp,
                                                            int run_tokens, int item_tokens) {
   constexpr int VPR = kBF16 ? 16 : 32;  // vectors per head row
@@ -191,7 +210,7 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q,
   constexpr int M = kAsyncVecs / 256;   // vectors per thread per tensor per item
   using Vec = typename std::conditional<kBF16, uint4, float4>::type;
   extern __shared__ __align__(16) uint8_t asm_raw[];
-  Vec* ring = reinterpret_cast<Vec*>(asm_raw);                                       // [stage][tensor][kAsyncVecs]
+  const Vec* ring = reinterpret_cast<const Vec*>(asm_raw);                            // [stage][tensor][kAsyncVecs]
   float2* cs = reinterpret_cast<float2*>(asm_raw + kAsyncStages * 2 * kAsyncVecs * 16);  // [kRunMax][64]
   __shared__ int8_t axis_s[64];
   const int tid = threadIdx.x;
@@ -199,37 +218,50 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q,
   const int tok_begin = blockIdx.x * run_tokens;
   const int tok_end = min(p.n_video, tok_begin + run_tokens);
   const int V = p.heads * VPR;
-  const int T = item_tokens;                 // T * V <= kAsyncVecs
-  const int g = tid & (VPR - 1);             // the thread's pair group (fixed: 256 % VPR == 0)
-  int tl_m[M], hoff_m[M];                    // token within the item, element offset within the token row
+  const int T = item_tokens;                           // T * V <= kAsyncVecs
+  const int g = tid & (VPR - 1);                       // the thread's pair group (fixed: 256 % VPR == 0)
+  const uint32_t row_bytes = static_cast<uint32_t>(p.row_stride) * ESZ;  // kRunMax rows stay below 2^31 bytes
+  const uint32_t item_bytes = static_cast<uint32_t>(T) * row_bytes;
+  int tl_m[M];          // token within the item (T: this slot is unused)
+  uint32_t boff_m[M];   // byte offset within the item
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     const int j = tid + 256 * m;
-    tl_m[m] = j < T * V ? j / V : T;         // T: this slot is unused
-    hoff_m[m] = ((j - (j / V) * V) / VPR) * 128 + g * (16 / ESZ);
+    const int tl = j / V;
+    tl_m[m] = j < T * V ? tl : T;
+    boff_m[m] = static_cast<uint32_t>(tl) * row_bytes + static_cast<uint32_t>(((j - tl * V) / VPR) * 128 * ESZ + g * 16);
   }
+  const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(asm_raw)) + 16u * tid;
   __syncthreads();
   bool rotated = false;
 #pragma unroll
   for (int e = 0; e < PPV; ++e) rotated |= axis_s[g * PPV + e] >= 0;
-  const int nt = (k != nullptr) ? 2 : 1;
   for (int f0 = tok_begin; f0 < tok_end; f0 += kRunMax) {
     const int nf = min(kRunMax, tok_end - f0);
     const int n_items = (nf + T - 1) / T;
-    auto fetch = [&](int i) {
+    const long long fill_elem = static_cast<long long>(f0) * p.row_stride;
+    char* const qf = q + fill_elem * ESZ;
+    char* const kf = kTwo ? k + fill_elem * ESZ : nullptr;
+    // The element offset a slot's vector starts at (bounds-checked build only).
+    const auto elem_of = [&](int tl, int m) {
+      return static_cast<long long>(f0 + tl) * p.row_stride + (boff_m[m] - tl_m[m] * row_bytes) / ESZ;
+    };
+    int stage_w = 0, stage_r = 0;
+    const auto fetch = [&](int i) {
       if (rotated && i < n_items) {
-        Vec* st = ring + (i % kAsyncStages) * 2 * kAsyncVecs;
+        const uint32_t st = ring_s + stage_w * (2 * kAsyncVecs * 16);
+        const uint32_t ib = static_cast<uint32_t>(i) * item_bytes;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
           const int tl = i * T + tl_m[m];
           if (tl_m[m] >= T || tl >= nf) continue;
-          const long long off = static_cast<long long>(f0 + tl) * p.row_stride + hoff_m[m];
-          if (!in_bounds(off, 16 / ESZ, p.extent, p.err)) continue;
-          for (int w = 0; w < nt; ++w)
-            cp_async16(&st[w * kAsyncVecs + tid + 256 * m], static_cast<const char*>(w ? k : q) + off * ESZ);
+          if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
+          cp_async16(st + m * 256 * 16, qf + ib + boff_m[m]);
+          if constexpr (kTwo) cp_async16(st + (kAsyncVecs + m * 256) * 16, kf + ib + boff_m[m]);
         }
       }
       cp_async_commit();  // one group per item, empty or not, so the group count stays uniform
+      stage_w = stage_w == kAsyncStages - 1 ? 0 : stage_w + 1;
     };
     for (int i = 0; i < kAsyncStages - 1; ++i) fetch(i);
     // cos/sin of the fill's tokens while the first items are in flight
@@ -252,14 +284,15 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q,
     for (int i = 0; i < n_items; ++i) {
       fetch(i + kAsyncStages - 1);
       cp_async_wait<kAsyncStages - 1>();  // this thread's copies of item i have landed
+      const Vec* st = ring + stage_r * 2 * kAsyncVecs + tid;
+      stage_r = stage_r == kAsyncStages - 1 ? 0 : stage_r + 1;
       if (!rotated) continue;
-      const Vec* st = ring + (i % kAsyncStages) * 2 * kAsyncVecs;
+      const uint32_t ib = static_cast<uint32_t>(i) * item_bytes;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         const int tl = i * T + tl_m[m];
         if (tl_m[m] >= T || tl >= nf) continue;
-        const long long off = static_cast<long long>(f0 + tl) * p.row_stride + hoff_m[m];
-        if (!in_bounds(off, 16 / ESZ, p.extent, p.err)) continue;
+        if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
         const float4* tab = reinterpret_cast<const float4*>(&cs[tl * 64 + g * PPV]);
         float cc[PPV], ss[PPV];
 #pragma unroll
@@ -270,23 +303,13 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q,
           cc[2 * h2 + 1] = t4.z;
           ss[2 * h2 + 1] = t4.w;
         }
-        for (int w = 0; w < nt; ++w) {
-          Vec v = st[w * kAsyncVecs + tid + 256 * m];
-          if constexpr (kBF16) {
-            uint32_t* u = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float x0 = __uint_as_float(u[e] << 16);
-              float x1 = __uint_as_float(u[e] & 0xFFFF0000u);
-              rope_rotate_pair(x0, x1, cc[e], ss[e]);
-              __nv_bfloat162 t2 = __floats2bfloat162_rn(x0, x1);
-              u[e] = *reinterpret_cast<const uint32_t*>(&t2);
-            }
-          } else {
-            rope_rotate_pair(v.x, v.y, cc[0], ss[0]);
-            rope_rotate_pair(v.z, v.w, cc[1], ss[1]);
-          }
-          reinterpret_cast<Vec*>(static_cast<char*>(w ? k : q))[off * ESZ / 16] = v;
+        Vec vq = st[256 * m];
+        rotate_vec<kBF16>(vq, cc, ss);
+        *reinterpret_cast<Vec*>(qf + ib + boff_m[m]) = vq;
+        if constexpr (kTwo) {
+          Vec vk = st[kAsyncVecs + 256 * m];
+          rotate_vec<kBF16>(vk, cc, ss);
+          *reinterpret_cast<Vec*>(kf + ib + boff_m[m]) = vk;
         }
       }
     }
@@ -296,6 +319,32 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(void* __restrict__ q,
 }
 
 constexpr int kAsyncSmem = kAsyncStages * 2 * kAsyncVecs * 16 + kRunMax * 64 * 8;
+
+template <bool kBF16, bool kTwo>
+cudaError_t launch_async(void* q, void* k, const RopeParams& p, const TwoPi& tp, int sms, int dev,
+                         cudaStream_t stream) {
+  static int configured[64] = {0};
+  if (!configured[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(rope3d_async_kernel<kBF16, kTwo>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAsyncSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_async_kernel<kBF16, kTwo>, 256, kAsyncSmem) !=
+          cudaSuccess ||
+      per_sm <= 0) {
+    (void)cudaGetLastError();
+    per_sm = 1;
+  }
+  const long long slots = static_cast<long long>(sms) * per_sm;
+  const int run = static_cast<int>((p.n_video + slots - 1) / slots);
+  const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);
+  const int item = kAsyncVecs / (p.heads * (kBF16 ? 16 : 32));
+  rope3d_async_kernel<kBF16, kTwo><<<grid, 256, kAsyncSmem, stream>>>(static_cast<char*>(q), static_cast<char*>(k), p,
+                                                                     tp, run, item);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -307,37 +356,16 @@ cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, c
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = 148;
   const int V = p.heads * (bf16_io ? 16 : 32);  // 16-byte vectors per token row
-  if (V <= kAsyncVecs && dev >= 0 && dev < 64) {
+  const int esz = bf16_io ? 2 : 4;
+  if (V <= kAsyncVecs && dev >= 0 && dev < 64 && p.row_stride * esz * kRunMax < (1ll << 31)) {
     // Async-copy form: one resident wave of CTAs (two per SM) with equal runs.
-    static int configured[2][64] = {{0}};
-    if (!configured[bf16_io][dev]) {
-      const cudaError_t e =
-          bf16_io ? cudaFuncSetAttribute(rope3d_async_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAsyncSmem)
-                  : cudaFuncSetAttribute(rope3d_async_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAsyncSmem);
-      if (e != cudaSuccess) return e;
-      configured[bf16_io][dev] = 1;
-    }
-    int per_sm = 0;
-    const cudaError_t e =
-        bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_async_kernel<true>, 256, kAsyncSmem)
-                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_async_kernel<false>, 256, kAsyncSmem);
-    if (e != cudaSuccess || per_sm <= 0) {
-      (void)cudaGetLastError();
-      per_sm = 1;
-    }
-    const long long slots = static_cast<long long>(sms) * per_sm;
-    const int run = static_cast<int>((p.n_video + slots - 1) / slots);
-    const unsigned grid = static_cast<unsigned>((p.n_video + run - 1) / run);
-    const int item = kAsyncVecs / V;
-    if (bf16_io)
-      rope3d_async_kernel<true><<<grid, 256, kAsyncSmem, stream>>>(q, k, p, tp, run, item);
-    else
-      rope3d_async_kernel<false><<<grid, 256, kAsyncSmem, stream>>>(q, k, p, tp, run, item);
-    return cudaGetLastError();
+    return bf16_io ? (k ? launch_async<true, true>(q, k, p, tp, sms, dev, stream)
+                        : launch_async<true, false>(q, k, p, tp, sms, dev, stream))
+                   : (k ? launch_async<false, true>(q, k, p, tp, sms, dev, stream)
+                        : launch_async<false, false>(q, k, p, tp, sms, dev, stream));
   }
-  // Rows wider than one item: the register-streaming form.
+  // Rows wider than one item (or a token stride too large for 32-bit offsets
+  // within a fill): the register-streaming form.
   int per_sm = 0;
   const cudaError_t e = bf16_io ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<true>, 256, 0)
                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope3d_run_kernel<false>, 256, 0);

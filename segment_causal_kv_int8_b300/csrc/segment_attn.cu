@@ -349,8 +349,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t peer = rank ^ 1u;
       int ri = 0, r_tma = 0;
       bool ok = true;
+      // This row's K and V scales of a cache tile (0 past its valid rows).
+      // They are loaded one tile ahead, so the global-load latency overlaps
+      // the conversion of the tile before instead of stalling it.
+      const long long scale_end = static_cast<long long>(p.block_heads) * p.scale_stride;
+      const auto load_scales = [&](int it_x, float& sk, float& sv) {
+        sk = sv = 0.0f;
+        if (it_x >= n_iter) return;
+        const TileInfo tx = tile_info(t_begin + it_x, p, kt);
+        if (!tx.cache || trow >= tx.valid) return;
+        const long long sidx = static_cast<long long>(bh) * p.scale_stride + tx.row0 + trow;
+        if (!in_bounds(sidx, 1, scale_end, p.err)) return;
+        sk = p.k_scale[sidx];
+        sv = p.v_scale[sidx];
+      };
+      float sc_next[2];
+      load_scales(0, sc_next[0], sc_next[1]);
       for (int it = 0; it < n_iter && ok; ++it) {
         const TileInfo ti = tile_info(t_begin + it, p, kt);
+        const float sc_tile[2] = {sc_next[0], sc_next[1]};
+        load_scales(it + 1, sc_next[0], sc_next[1]);
         for (int kv = 0; kv < 2; ++kv) {
           const int r = 2 * it + kv, s = r % L::NS, u = r / L::NS;
           uint64_t* fb = &bars[L::bRingFull + s];
@@ -373,12 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
           const int si = ri % L::NI, ui = ri / L::NI;
-          const float* sp = kv ? p.v_scale : p.k_scale;
-          const long long sidx = static_cast<long long>(bh) * p.scale_stride + ti.row0 + trow;
-          const float sc = (trow < ti.valid && in_bounds(sidx, 1, static_cast<long long>(p.block_heads) * p.scale_stride,
-                                                          p.err))
-                               ? sp[sidx]
-                               : 0.0f;
+          const float sc = sc_tile[kv];
           if (!warp_wait(&bars[L::bStageFull + si], ui & 1, ab, p.err)) {
             ok = false;
             break;
