@@ -415,7 +415,11 @@ nomas_status nomas_segment_attn_noalloc(const nomas_kvcache* cache, int32_t bloc
  *   n_cam        camera tokens per latent frame, 1 .. 16
  *   softmax_scale s > 0
  *   out          device bf16 [frames * grid_h * grid_w][heads][128]
- * float32 arithmetic, bf16 output.  NOMAS_ERR_UNSUPPORTED for n_cam > 16.
+ * All four pointers 16-byte aligned.  Scores and the weighted sum of V
+ * accumulate in float32 on the tensor cores; the softmax runs in float32 and
+ * its weights are rounded to bf16 for the weighted sum, as in
+ * nomas_segment_attn; bf16 output.  NOMAS_ERR_UNSUPPORTED for n_cam > 16 or
+ * more than 65535 heads or frames.
  */
 nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam, const void* v_cam,
                                      int32_t frames, int32_t grid_h, int32_t grid_w,

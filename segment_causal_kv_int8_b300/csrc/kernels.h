@@ -131,7 +131,14 @@ struct CameraAttnParams {
   uint32_t* err;                 // device error word (checked build)
 };
 
-cudaError_t launch_camera_attn(const CameraAttnParams& p, cudaStream_t stream);
+// TMA maps (128 dims, heads, tokens, frames) of the query rows and the output
+// (tokens = tpf), and of the camera K and V (tokens = n_cam); boxes of 64
+// dims x 1 head x 128 (16 for camera) tokens x 1 frame, 128-byte swizzle.
+struct CameraTensorMaps {
+  CUtensorMap q, k, v, o;
+};
+
+cudaError_t launch_camera_attn(const CameraTensorMaps& tm, const CameraAttnParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention
 struct AttnTensorMaps {

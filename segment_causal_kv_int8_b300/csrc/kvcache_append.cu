@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(256, kF32In ? 4 : 8) append_kernel(const __gri
   for (int r = 0; r < kAppendTokens; ++r) {
     const int n = n0 + r;
     if (n >= p.n_tokens) break;
-    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    const int f = fast_div(n, p.tpf_div);  // written frames never exceed the ring, so one wrap at most
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
@@ -289,9 +289,9 @@ __global__ void __launch_bounds__(256, K != kCacheBF16 ? 5 : 8) append8_kernel(c
   for (int r = 0; r < 2; ++r) {
     const int row = r0 + (threadIdx.x >> 3) + 32 * r;
     if (row >= rows) break;  // rows of one 8-lane group: uniform
-    const int n = static_cast<int>(static_cast<unsigned>(row) / static_cast<unsigned>(p.heads));
+    const int n = fast_div(row, p.heads_div);
     const int h = row - n * p.heads;
-    const int f = static_cast<int>(static_cast<unsigned>(n) / static_cast<unsigned>(p.tpf));  // one wrap at most
+    const int f = fast_div(n, p.tpf_div);  // written frames never exceed the ring, so one wrap at most
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
@@ -395,9 +395,9 @@ __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const 
       // Both 16-lane groups of a warp take the same number of rows.
       for (int r = grp; r < ((rows + 15) & ~15); r += 16) {
         if (r < rows) {
-          const int tok = r / p.heads, h = r - tok * p.heads;
+          const int tok = fast_div(r, p.heads_div), h = r - tok * p.heads;
           float x[8];
-          const uint8_t* src = stage + ((static_cast<long long>(tok) * p.heads + h) * 128 + 8 * g) * esz;
+          const uint8_t* src = stage + (r * 128 + 8 * g) * esz;  // row r = tok * heads + h of the chunk
           if constexpr (kF32In) {
             const float4 a = *reinterpret_cast<const float4*>(src);
             const float4 c = *reinterpret_cast<const float4*>(src + 16);
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) append_staged_kernel(const 
             }
           }
           const int n = n0 + tok;
-          const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+          const int f = fast_div(n, p.tpf_div);  // written frames never exceed the ring, so one wrap at most
           int slot_frame = p.base_slot_frame + f;
           if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
           const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant_
       const int a = rp.axis[pair];
       float c = 1.0f, sn = 0.0f;
       if (n < p.n_tokens && a >= 0) {
-        const int f = n / p.tpf;
+        const int f = fast_div(n, p.tpf_div);
         const int within = n - f * p.tpf;
         const int row = within / rp.grid_w;
         const float pos = a == 0 ? static_cast<float>(rp.t0 + f)
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant_
         rope_rotate_pair(x[r][2 * e], x[r][2 * e + 1], t.x, t.y);
       }
     }
-    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    const int f = fast_div(n, p.tpf_div);  // written frames never exceed the ring, so one wrap at most
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = plane * p.cap_slots + static_cast<long long>(slot_frame) * p.tpf + (n - f * p.tpf);
@@ -520,19 +520,19 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
   const unsigned gmask = 0xFFu << (threadIdx.x & 24);
   const int tensor = blockIdx.z & 1;
   const int b = blockIdx.z >> 1;
-  const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
-  const long long r0 = static_cast<long long>(blockIdx.x) * kRope8Rows;
-  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(tensor ? p.v : p.k) + b * p.block_stride +
-                             static_cast<long long>(p.first_frame) * p.tpf * p.heads * 128;
+  // rows = n_tokens * heads < 2^31 (checked by the launcher)
+  const int rows = p.n_tokens * p.heads;
+  const int r0 = static_cast<int>(blockIdx.x) * kRope8Rows;
+  const long long src0 = b * p.block_stride + static_cast<long long>(p.first_frame) * p.tpf * p.heads * 128;
+  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(tensor ? p.v : p.k) + src0;
   uint4 w[2][2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const long long row = r0 + (threadIdx.x >> 3) + 32 * r;
+    const int row = r0 + (threadIdx.x >> 3) + 32 * r;
     if (row < rows) {
-      const long long off = b * p.block_stride + static_cast<long long>(p.first_frame) * p.tpf * p.heads * 128 +
-                            row * 128 + 16 * g;
+      const long long off = src0 + static_cast<long long>(row) * 128 + 16 * g;
       if (in_bounds(off, 16, p.src_extent, p.err)) {
-        const uint4* q = reinterpret_cast<const uint4*>(src + row * 128 + 16 * g);
+        const uint4* q = reinterpret_cast<const uint4*>(src + static_cast<long long>(row) * 128 + 16 * g);
         w[r][0] = q[0];
         w[r][1] = q[1];
       } else {
@@ -540,16 +540,16 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
       }
     }
   }
-  const int tok0 = static_cast<int>(r0 / p.heads);
+  const int tok0 = fast_div(r0, p.heads_div);
   if (tensor == 0) {
-    const int n_tok = static_cast<int>(min(rows - 1, r0 + kRope8Rows - 1) / p.heads) - tok0 + 1;
+    const int n_tok = fast_div(min(rows - 1, r0 + kRope8Rows - 1), p.heads_div) - tok0 + 1;
     for (int i = threadIdx.x; i < n_tok * kRopeMaxPairs; i += blockDim.x) {
       const int t = i / kRopeMaxPairs, pair = i - t * kRopeMaxPairs;
       const int n = tok0 + t;
       const int a = rp.axis[pair];
       float c = 1.0f, sn = 0.0f;
       if (a >= 0) {
-        const int f = n / p.tpf;
+        const int f = fast_div(n, p.tpf_div);
         const int within = n - f * p.tpf;
         const int hrow = within / rp.grid_w;
         const float pos = a == 0 ? static_cast<float>(rp.t0 + f)
@@ -562,10 +562,10 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
   }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const long long row = r0 + (threadIdx.x >> 3) + 32 * r;
+    const int row = r0 + (threadIdx.x >> 3) + 32 * r;
     if (row >= rows) break;  // rows of one 8-lane group: uniform
-    const int n = static_cast<int>(row / p.heads);
-    const int h = static_cast<int>(row - static_cast<long long>(n) * p.heads);
+    const int n = fast_div(row, p.heads_div);
+    const int h = row - n * p.heads;
     const uint32_t u[8] = {w[r][0].x, w[r][0].y, w[r][0].z, w[r][0].w, w[r][1].x, w[r][1].y, w[r][1].z, w[r][1].w};
     float x[16];
 #pragma unroll
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
         rope_rotate_pair(x[2 * e], x[2 * e + 1], t.x, t.y);
       }
     }
-    const int f = n / p.tpf;  // written frames never exceed the ring, so one wrap at most
+    const int f = fast_div(n, p.tpf_div);  // written frames never exceed the ring, so one wrap at most
     int slot_frame = p.base_slot_frame + f;
     if (slot_frame >= p.capacity_frames) slot_frame -= p.capacity_frames;
     const long long dst_row = (static_cast<long long>(b) * p.heads + h) * p.cap_slots +
@@ -605,20 +605,31 @@ cudaError_t launch_append_rope(bool f32_in, int kind, const AppendParams& p, con
   if (p.n_tokens <= 0 || p.blocks <= 0 || p.heads <= 0) return cudaSuccess;
   if (kind != kCacheBF16 && kind != kCacheInt8 && kind != kCacheFp8) return cudaErrorInvalidValue;
   const TwoPi tp = rope_two_pi();
-  if (f32_in) {
+  const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
+  if (f32_in || rows >= 0x7FFFFFFFLL - kRope8Rows) {
+    // Float32 input, or more rows than 32-bit row indices cover: 16 lanes per
+    // row, a CTA per 8 tokens and 16 heads.
     const dim3 grid(static_cast<unsigned>((p.n_tokens + kRopeAppendTokens - 1) / kRopeAppendTokens),
                     static_cast<unsigned>((p.heads + 15) / 16), static_cast<unsigned>(2 * p.blocks));
     if (grid.y > 65535 || grid.z > 65535) return cudaErrorInvalidValue;
-    if (kind == kCacheInt8)
-      append_rope_kernel<true, kCacheInt8><<<grid, 256, 0, stream>>>(p, rp, tp);
-    else if (kind == kCacheFp8)
-      append_rope_kernel<true, kCacheFp8><<<grid, 256, 0, stream>>>(p, rp, tp);
-    else
-      append_rope_kernel<true, kCacheBF16><<<grid, 256, 0, stream>>>(p, rp, tp);
+    if (f32_in) {
+      if (kind == kCacheInt8)
+        append_rope_kernel<true, kCacheInt8><<<grid, 256, 0, stream>>>(p, rp, tp);
+      else if (kind == kCacheFp8)
+        append_rope_kernel<true, kCacheFp8><<<grid, 256, 0, stream>>>(p, rp, tp);
+      else
+        append_rope_kernel<true, kCacheBF16><<<grid, 256, 0, stream>>>(p, rp, tp);
+    } else {
+      if (kind == kCacheInt8)
+        append_rope_kernel<false, kCacheInt8><<<grid, 256, 0, stream>>>(p, rp, tp);
+      else if (kind == kCacheFp8)
+        append_rope_kernel<false, kCacheFp8><<<grid, 256, 0, stream>>>(p, rp, tp);
+      else
+        append_rope_kernel<false, kCacheBF16><<<grid, 256, 0, stream>>>(p, rp, tp);
+    }
   } else {
-    const long long rows = static_cast<long long>(p.n_tokens) * p.heads;
     const long long cta = (rows + kRope8Rows - 1) / kRope8Rows;
-    if (cta > 0x7FFFFFFFLL || 2LL * p.blocks > 65535) return cudaErrorInvalidValue;
+    if (2LL * p.blocks > 65535) return cudaErrorInvalidValue;
     const dim3 grid8(static_cast<unsigned>(cta), 1, static_cast<unsigned>(2 * p.blocks));
     if (kind == kCacheInt8)
       append8_rope_kernel<kCacheInt8><<<grid8, 256, 0, stream>>>(p, rp, tp);

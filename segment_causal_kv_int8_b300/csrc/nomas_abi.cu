@@ -132,6 +132,21 @@ nomas_status encode3d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64
   return r == CUDA_SUCCESS ? NOMAS_OK : NOMAS_ERR_CUDA;
 }
 
+// Encode a 4D tiled TMA descriptor (dims/strides innermost first, strides in bytes).
+nomas_status encode4d(CUtensorMap* m, void* base, const uint64_t (&d)[4], const uint64_t (&s)[3],
+                      const uint32_t (&b)[4]) {
+  EncodeTiledFn fn = nullptr;
+  nomas_status st = encoder(&fn);
+  if (st != NOMAS_OK) return st;
+  const cuuint64_t dims[4] = {d[0], d[1], d[2], d[3]};
+  const cuuint64_t strides[3] = {s[0], s[1], s[2]};
+  const cuuint32_t box[4] = {b[0], b[1], b[2], b[3]};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NOMAS_OK : NOMAS_ERR_CUDA;
+}
+
 // Work plan of one attention call (see AttnParams): units of one head x 256
 // query rows (BF16 cache) or x 512 rows in a CTA pair (one-byte caches);
 // units 0 .. n_full-1 run whole, every later unit in `splits` pieces of its
@@ -486,7 +501,7 @@ NOMAS_API nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam,
                                                float softmax_scale, void* out, cudaStream_t stream) {
   if (frames < 0 || grid_h <= 0 || grid_w <= 0 || heads <= 0 || n_cam <= 0) return NOMAS_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || !isfinite(softmax_scale)) return NOMAS_ERR_INVALID_ARG;
-  if (n_cam > 16 || heads > 65535 * 4 || frames > 65535) return NOMAS_ERR_UNSUPPORTED;
+  if (n_cam > 16 || heads > 65535 || frames > 65535) return NOMAS_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(grid_h) * grid_w > (int64_t(1) << 30)) return NOMAS_ERR_UNSUPPORTED;
   if (frames == 0) return NOMAS_OK;
   if (q == nullptr || k_cam == nullptr || v_cam == nullptr || out == nullptr) return NOMAS_ERR_INVALID_ARG;
@@ -503,7 +518,23 @@ NOMAS_API nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam,
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.err = nullptr;
   if (device_state(&p.err, nullptr) != NOMAS_OK) p.err = nullptr;
-  return from_cuda(launch_camera_attn(p, stream));
+  // Rows [frame][token][head][128]: the token extent of the query and output
+  // maps is one frame's tpf, of the camera maps n_cam, so a box never reaches
+  // into the next frame.
+  const uint64_t H = static_cast<uint64_t>(heads), T = static_cast<uint64_t>(p.tpf), C = static_cast<uint64_t>(n_cam);
+  CameraTensorMaps tm;
+  nomas_status st = encode4d(&tm.q, const_cast<void*>(q), {128, H, T, static_cast<uint64_t>(frames)},
+                             {256, H * 256, T * H * 256}, {64, 1, 128, 1});
+  if (st == NOMAS_OK)
+    st = encode4d(&tm.o, out, {128, H, T, static_cast<uint64_t>(frames)}, {256, H * 256, T * H * 256}, {64, 1, 128, 1});
+  if (st == NOMAS_OK)
+    st = encode4d(&tm.k, const_cast<void*>(k_cam), {128, H, C, static_cast<uint64_t>(frames)},
+                  {256, H * 256, C * H * 256}, {64, 1, 16, 1});
+  if (st == NOMAS_OK)
+    st = encode4d(&tm.v, const_cast<void*>(v_cam), {128, H, C, static_cast<uint64_t>(frames)},
+                  {256, H * 256, C * H * 256}, {64, 1, 16, 1});
+  if (st != NOMAS_OK) return st;
+  return from_cuda(launch_camera_attn(tm, p, stream));
 }
 
 NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream) {
