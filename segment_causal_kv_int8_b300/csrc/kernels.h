@@ -49,6 +49,8 @@ struct RopeParams {
   long long t0;
   long long extent;              // elements of Q (and K) the call may touch (checked build)
   uint32_t* err;                 // device error word (checked build)
+  FastDiv tpf_div;               // n / tpf
+  FastDiv gw_div;                // n / grid_w
 };
 
 cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, cudaStream_t stream);

@@ -475,9 +475,9 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const __grid_constant_
       if (n < p.n_tokens && a >= 0) {
         const int f = fast_div(n, p.tpf_div);
         const int within = n - f * p.tpf;
-        const int row = within / rp.grid_w;
-        const float pos = a == 0 ? static_cast<float>(rp.t0 + f)
-                                 : static_cast<float>(a == 1 ? row : within - row * rp.grid_w);
+        const int row = fast_div(within, rp.gw_div);
+        const float pos = static_cast<float>(a == 0 ? static_cast<int>(rp.t0) + f
+                                                    : (a == 1 ? row : within - row * rp.grid_w));
         sincosf(rope_reduced_angle(pos, rp.f_hi[pair], rp.f_lo[pair], tp), &sn, &c);
       }
       cs[r][pair] = make_float2(c, sn);
@@ -551,9 +551,9 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
       if (a >= 0) {
         const int f = fast_div(n, p.tpf_div);
         const int within = n - f * p.tpf;
-        const int hrow = within / rp.grid_w;
-        const float pos = a == 0 ? static_cast<float>(rp.t0 + f)
-                                 : static_cast<float>(a == 1 ? hrow : within - hrow * rp.grid_w);
+        const int hrow = fast_div(within, rp.gw_div);
+        const float pos = static_cast<float>(a == 0 ? static_cast<int>(rp.t0) + f
+                                                    : (a == 1 ? hrow : within - hrow * rp.grid_w));
         sincosf(rope_reduced_angle(pos, rp.f_hi[pair], rp.f_lo[pair], tp), &sn, &c);
       }
       cs[t][pair] = make_float2(c, sn);

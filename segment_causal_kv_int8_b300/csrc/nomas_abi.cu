@@ -335,6 +335,8 @@ NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, i
   p.row_stride = row_stride_elems;
   p.tpf = grid_h * grid_w;
   p.grid_w = grid_w;
+  p.tpf_div = make_fast_div(static_cast<uint32_t>(p.tpf));
+  p.gw_div = make_fast_div(static_cast<uint32_t>(grid_w));
   p.t0 = t0;
   p.extent = (static_cast<long long>(n_video) - 1) * row_stride_elems + static_cast<long long>(heads) * head_dim;
   p.err = nullptr;
@@ -398,6 +400,8 @@ nomas_status append_impl(nomas_kvcache* cache, const void* k, const void* v, nom
       rp.t0 = cache->total_frames + first;  // absolute latent frame of the first written frame
       rp.tpf = p.tpf;
       rp.grid_w = cache->grid_w;
+      rp.tpf_div = p.tpf_div;
+      rp.gw_div = make_fast_div(static_cast<uint32_t>(cache->grid_w));
       rp.heads = cache->heads;
       rp.n_video = p.n_tokens;
       rp.row_stride = static_cast<long long>(cache->heads) * cache->head_dim;

@@ -137,11 +137,12 @@ __global__ void __launch_bounds__(256) rope3d_run_kernel(void* __restrict__ q, v
       float c = 1.0f, sn = 0.0f;
       if (a >= 0) {
         const int tok = f0 + t;
-        const int frame = tok / p.tpf;
+        const int frame = fast_div(tok, p.tpf_div);
         const int within = tok - frame * p.tpf;
-        const int row = within / p.grid_w;
-        const float pos = a == 0 ? static_cast<float>(p.t0 + frame)
-                                 : static_cast<float>(a == 1 ? row : within - row * p.grid_w);
+        const int row = fast_div(within, p.gw_div);
+        // positions stay below 2^24 (checked by the caller): 32-bit integer to float is exact
+        const float pos = static_cast<float>(a == 0 ? static_cast<int>(p.t0) + frame
+                                                    : (a == 1 ? row : within - row * p.grid_w));
         sincosf(rope_reduced_angle(pos, p.f_hi[pair], p.f_lo[pair], tp), &sn, &c);
       }
       cs[e] = make_float2(c, sn);
@@ -271,11 +272,12 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q,
       float c = 1.0f, sn = 0.0f;
       if (a >= 0) {
         const int tok = f0 + t;
-        const int frame = tok / p.tpf;
+        const int frame = fast_div(tok, p.tpf_div);
         const int within = tok - frame * p.tpf;
-        const int row = within / p.grid_w;
-        const float pos = a == 0 ? static_cast<float>(p.t0 + frame)
-                                 : static_cast<float>(a == 1 ? row : within - row * p.grid_w);
+        const int row = fast_div(within, p.gw_div);
+        // positions stay below 2^24 (checked by the caller): 32-bit integer to float is exact
+        const float pos = static_cast<float>(a == 0 ? static_cast<int>(p.t0) + frame
+                                                    : (a == 1 ? row : within - row * p.grid_w));
         sincosf(rope_reduced_angle(pos, p.f_hi[pair], p.f_lo[pair], tp), &sn, &c);
       }
       cs[e] = make_float2(c, sn);
