@@ -541,6 +541,7 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
     # inputs in HBM, no other kernel's dirty lines to write back): the
     # kernels' own bandwidth, next to their times inside the step.
     iso = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(min(steps, 50))]
+    torch.cuda._sleep(int(2e6) * len(iso))  # hold the stream while the host enqueues, as for the steps
     for ev in iso:
         restage()
         cache.reset(zero_memory=False)

@@ -248,17 +248,34 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q,
       return static_cast<long long>(f0 + tl) * p.row_stride + (boff_m[m] - tl_m[m] * row_bytes) / ESZ;
     };
     int stage_w = 0, stage_r = 0;
+    // Item i uses every slot of every thread when the items tile the ring
+    // exactly and i is not the fill's partial last item: such items take a
+    // path without per-slot checks.
+    const bool dense = T * V == kAsyncVecs;
     const auto fetch = [&](int i) {
       if (rotated && i < n_items) {
         const uint32_t st = ring_s + stage_w * (2 * kAsyncVecs * 16);
         const uint32_t ib = static_cast<uint32_t>(i) * item_bytes;
+        const char* qb = qf + ib;
+        const char* kb = kTwo ? kf + ib : nullptr;
+        const auto copy_slot = [&](int m) {
+          cp_async16(st + m * 256 * 16, qb + boff_m[m]);
+          if constexpr (kTwo) cp_async16(st + (kAsyncVecs + m * 256) * 16, kb + boff_m[m]);
+        };
+        if (dense && (i + 1) * T <= nf) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          const int tl = i * T + tl_m[m];
-          if (tl_m[m] >= T || tl >= nf) continue;
-          if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
-          cp_async16(st + m * 256 * 16, qf + ib + boff_m[m]);
-          if constexpr (kTwo) cp_async16(st + (kAsyncVecs + m * 256) * 16, kf + ib + boff_m[m]);
+          for (int m = 0; m < M; ++m) {
+            if (!in_bounds(elem_of(i * T + tl_m[m], m), 16 / ESZ, p.extent, p.err)) continue;
+            copy_slot(m);
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            const int tl = i * T + tl_m[m];
+            if (tl_m[m] >= T || tl >= nf) continue;
+            if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
+            copy_slot(m);
+          }
         }
       }
       cp_async_commit();  // one group per item, empty or not, so the group count stays uniform
@@ -290,11 +307,9 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q,
       stage_r = stage_r == kAsyncStages - 1 ? 0 : stage_r + 1;
       if (!rotated) continue;
       const uint32_t ib = static_cast<uint32_t>(i) * item_bytes;
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const int tl = i * T + tl_m[m];
-        if (tl_m[m] >= T || tl >= nf) continue;
-        if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
+      char* qb = qf + ib;
+      char* kb = kTwo ? kf + ib : nullptr;
+      const auto rotate_slot = [&](int m, int tl) {
         const float4* tab = reinterpret_cast<const float4*>(&cs[tl * 64 + g * PPV]);
         float cc[PPV], ss[PPV];
 #pragma unroll
@@ -307,11 +322,27 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q,
         }
         Vec vq = st[256 * m];
         rotate_vec<kBF16>(vq, cc, ss);
-        *reinterpret_cast<Vec*>(qf + ib + boff_m[m]) = vq;
+        *reinterpret_cast<Vec*>(qb + boff_m[m]) = vq;
         if constexpr (kTwo) {
           Vec vk = st[kAsyncVecs + 256 * m];
           rotate_vec<kBF16>(vk, cc, ss);
-          *reinterpret_cast<Vec*>(kf + ib + boff_m[m]) = vk;
+          *reinterpret_cast<Vec*>(kb + boff_m[m]) = vk;
+        }
+      };
+      if (dense && (i + 1) * T <= nf) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const int tl = i * T + tl_m[m];
+          if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
+          rotate_slot(m, tl);
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const int tl = i * T + tl_m[m];
+          if (tl_m[m] >= T || tl >= nf) continue;
+          if (!in_bounds(elem_of(tl, m), 16 / ESZ, p.extent, p.err)) continue;
+          rotate_slot(m, tl);
         }
       }
     }
