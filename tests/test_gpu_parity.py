@@ -79,6 +79,28 @@ def test_rope3d_padded_token_rows(io_dtype):
         assert bool((wide[:, wl.heads:] == 7.0).all())
 
 
+@pytest.mark.parametrize("heads", [8, 32, 64, 65])
+def test_rope3d_head_counts(heads):
+    # 8, 32 and 64 bf16 heads tile the copy ring exactly (8, 2 and 1 tokens per
+    # item: full items skip the per-slot checks, a fill's partial last item
+    # keeps them); 65 heads are wider than one item (the register-streaming
+    # kernel).  2760 video tokens give each CTA a run of about ten tokens, so
+    # full and partial items both occur.  Q and K both rotated, against the oracle.
+    wl = small_variant(CONFIGS["c2_bf16_hist8"], heads=heads, grid_h=23, grid_w=40, cur_frames=3, n_text=5,
+                       seed=90 + heads)
+    q, k, _ = current_qkv(wl)
+    qd, kd = to_dev(q, wl.io_dtype), to_dev(k, wl.io_dtype)
+    nomas.rope3d(qd, kd, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+    nv = wl.n_video
+    for dev, host in ((qd, q), (kd, k)):
+        ref = o_rope.rope3d_segment(host, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
+        got = f64(dev)
+        np.testing.assert_array_equal(got[nv:], host[nv:].astype(np.float64))
+        d = np.abs(got[:nv] - ref[:nv])
+        vec_inf = np.max(np.abs(ref[:nv]), axis=2, keepdims=True)
+        assert np.all(d <= 2.0 ** -8 * np.abs(ref[:nv]) + ROPE_REL * vec_inf)
+
+
 def test_rope3d_large_frame_index_and_odd_split():
     wl = small_variant(CONFIGS["c1_tiny"], io_dtype="f32", grid_h=3, grid_w=5, cur_frames=3, n_text=2)
     q, k, _ = current_qkv(wl)
