@@ -297,7 +297,10 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q,
                                                     : (a == 1 ? row : within - row * p.grid_w));
         sincosf(rope_reduced_angle(pos, p.f_hi[pair], p.f_lo[pair], tp), &sn, &c);
       }
-      cs[e] = make_float2(c, sn);
+      // Stored so that each pair group's 16-byte table chunks h2 = 0, 1 sit in
+      // rows of 16 consecutive groups: a warp's table reads are contiguous
+      // 256-byte spans, free of bank conflicts.
+      cs[t * 64 + ((pair % PPV) >> 1) * 32 + 2 * (pair / PPV) + (pair & 1)] = make_float2(c, sn);
     }
     __syncthreads();
     for (int i = 0; i < n_items; ++i) {
@@ -310,11 +313,10 @@ __global__ void __launch_bounds__(256) rope3d_async_kernel(char* __restrict__ q,
       char* qb = qf + ib;
       char* kb = kTwo ? kf + ib : nullptr;
       const auto rotate_slot = [&](int m, int tl) {
-        const float4* tab = reinterpret_cast<const float4*>(&cs[tl * 64 + g * PPV]);
         float cc[PPV], ss[PPV];
 #pragma unroll
         for (int h2 = 0; h2 < PPV / 2; ++h2) {
-          const float4 t4 = tab[h2];
+          const float4 t4 = *reinterpret_cast<const float4*>(&cs[tl * 64 + h2 * 32 + 2 * g]);
           cc[2 * h2] = t4.x;
           ss[2 * h2] = t4.y;
           cc[2 * h2 + 1] = t4.z;
