@@ -8,10 +8,13 @@
 // the cache (the "Schreiben des KV-Cache" stage, section "Zeiten").
 //
 // One row = the head_dim = 128 values of one (tensor, block, head, token).
-// 16 threads own a row (8 values each: a 16-byte bf16 or 32-byte f32 load),
-// reduce the absmax with four shuffles and write 8 code bytes each plus the
-// row's scale.  A CTA covers a few consecutive tokens of 16 heads, so it reads
-// whole token rows and writes runs of consecutive ring slots per head.
+// Bf16 input (append8_kernel): 8 lanes own a row (16 values each, two 16-byte
+// loads), reduce the absmax with three shuffles and write 16 code bytes each
+// plus the row's scale; a CTA takes 64 consecutive (token, head) rows, one
+// contiguous 16 KB range of the input.  Float32 input (append_kernel): 16
+// lanes per row, a CTA per two tokens and 16 heads.  Large appends stream
+// through shared memory instead (append_staged_kernel).  A row's token, head
+// and frame come from multiply-shift division by run-time constants.
 //
 // Codec bits (identical to the reference definition): scale = fl32(m / 127),
 // inv = fl32(127 / m) (IEEE round-to-nearest divisions), code =
@@ -515,7 +518,7 @@ constexpr int kRope8MaxTokens = kRope8Rows + 1;  // tokens a 64-row range can to
 template <int K>
 __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_constant__ AppendParams p,
                                                               const __grid_constant__ RopeParams rp, TwoPi tp) {
-  __shared__ float2 cs[kRope8MaxTokens][kRopeMaxPairs];
+  __shared__ __align__(16) float2 cs[kRope8MaxTokens][kRopeMaxPairs];
   const int g = threadIdx.x & 7;
   const unsigned gmask = 0xFFu << (threadIdx.x & 24);
   const int tensor = blockIdx.z & 1;
@@ -556,7 +559,9 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
                                                     : (a == 1 ? hrow : within - hrow * rp.grid_w));
         sincosf(rope_reduced_angle(pos, rp.f_hi[pair], rp.f_lo[pair], tp), &sn, &c);
       }
-      cs[t][pair] = make_float2(c, sn);
+      // Lane g's pairs 8g .. 8g+7 as four 16-byte chunks, chunk i of all eight
+      // lanes side by side: a group's table reads are contiguous 128 bytes.
+      cs[t][((pair & 7) >> 1) * 16 + 2 * (pair >> 3) + (pair & 1)] = make_float2(c, sn);
     }
     __syncthreads();  // tensor is uniform over the CTA
   }
@@ -575,9 +580,10 @@ __global__ void __launch_bounds__(256, 4) append8_rope_kernel(const __grid_const
     }
     if (tensor == 0) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 t = cs[n - tok0][8 * g + e];
-        rope_rotate_pair(x[2 * e], x[2 * e + 1], t.x, t.y);
+      for (int i = 0; i < 4; ++i) {
+        const float4 t = *reinterpret_cast<const float4*>(&cs[n - tok0][16 * i + 2 * g]);
+        rope_rotate_pair(x[4 * i], x[4 * i + 1], t.x, t.y);
+        rope_rotate_pair(x[4 * i + 2], x[4 * i + 3], t.z, t.w);
       }
     }
     const int f = fast_div(n, p.tpf_div);  // written frames never exceed the ring, so one wrap at most

@@ -5,18 +5,20 @@
 // into contiguous chunks per axis; pair (x[o+2i], x[o+2i+1]) of the chunk of
 // axis a rotates by pos_a * f_{a,i}, f_{a,i} = theta^(-2i/d_a).
 //
-// HBM-bound elementwise kernel.  Each CTA takes a contiguous run of tokens:
-// it first computes the cos/sin of every (token, pair) of the run once into
-// shared memory (angle arithmetic in rope_math.cuh; shared by every head and
-// by Q and K), then streams the rows of Q and K as 16-byte vectors, one
-// vector per thread per tensor and token.  A thread works in items of two
-// tokens (four 16-byte loads) with two buffers: the first item's loads go out
-// before the table is computed, and each next item's loads are in flight
-// while the current one is rotated.  The grid is one resident wave of CTAs
-// with equal token runs, so no partial last wave.  A thread's vectors always hold the same
-// rotary pairs, so its table reads are one or two 16-byte loads.  The cos/sin
-// of a pair depend only on its position and frequency, so the rotation is bit
-// for bit what per-element evaluation gives.
+// HBM-bound elementwise kernel.  The grid is one resident wave of CTAs, each
+// taking an equal run of consecutive tokens (no partial last wave).  A CTA
+// first computes the cos/sin of every (token, pair) of its run into shared
+// memory (angle arithmetic in rope_math.cuh; shared by every head and by Q
+// and K), then streams the rows of Q and K as 16-byte vectors.  A thread's
+// vectors always hold the same rotary pairs of some head, so its table reads
+// are one or two 16-byte loads.  The cos/sin of a pair depend only on its
+// position and frequency, so the rotation is bit for bit what per-element
+// evaluation gives.
+//
+// Two forms: rope3d_async_kernel (token rows of up to 1024 vectors) copies
+// each thread's vectors through a cp.async ring in shared memory;
+// rope3d_run_kernel (wider rows) double-buffers items of two tokens' vectors
+// in registers, the first item's loads issued before the table is computed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
