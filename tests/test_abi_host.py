@@ -128,6 +128,29 @@ def test_invalid_calls_return_status_without_launching():
     assert nomas.nomas_kvcache_append(ctypes.byref(d), None, None, nomas.NOMAS_BF16, 0, 0, None) == nomas.NOMAS_OK
 
 
+def test_camera_cross_attention_validates_before_launching():
+    cam = nomas.nomas_camera_cross_attn
+    # frames, grid_h, grid_w, heads, n_cam, scale; fake 256-aligned pointers never reach a launch
+    ok = dict(frames=2, gh=3, gw=4, heads=2, n_cam=4, scale=0.1)
+
+    def call(q=256, k=256, v=256, out=256, **kw):
+        a = dict(ok, **kw)
+        return cam(q, k, v, a["frames"], a["gh"], a["gw"], a["heads"], a["n_cam"], a["scale"], out, None)
+
+    assert call(n_cam=0) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(n_cam=17) == nomas.NOMAS_ERR_UNSUPPORTED
+    assert call(heads=0) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(heads=65536) == nomas.NOMAS_ERR_UNSUPPORTED   # one grid row per head
+    assert call(frames=-1) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(frames=65536) == nomas.NOMAS_ERR_UNSUPPORTED
+    assert call(scale=0.0) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(q=None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(out=None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert call(k=264) == nomas.NOMAS_ERR_INVALID_ARG          # not 16-byte aligned (TMA)
+    assert call(frames=0, q=None, k=None, v=None, out=None) == nomas.NOMAS_OK  # nothing to do
+
+
 def _round256(x):
     return -(-x // 256) * 256
 
