@@ -588,10 +588,10 @@ def summarize_block_call(wl, m, world, steps, peaks, append_rope=False, camera=0
     el = {}
     name = "kvcache_append_rope" if append_rope else "kvcache_append"
     el[name] = hbm_entry(append_bytes(wl), 1e3 * statistics.mean(m["append_ms"]), hbm, len(wl.cache_frames_hist),
-                         isolated=hbm_entry(append_bytes(wl), 1e3 * statistics.median(m["append_iso_ms"]), hbm,
+                         isolated=hbm_entry(append_bytes(wl), 1e3 * statistics.mean(m["append_iso_ms"]), hbm,
                                             len(wl.cache_frames_hist), timing="alone after an L2 eviction"))
     el["rope3d"] = hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_ms"]), hbm, 1,
-                             isolated=hbm_entry(rope_bytes(wl), 1e3 * statistics.median(m["rope_iso_ms"]), hbm, 1,
+                             isolated=hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_iso_ms"]), hbm, 1,
                                                 timing="alone after an L2 eviction"))
     if camera:
         nbytes = 2 * wl.n_video * wl.heads * wl.head_dim * 2 + 2 * wl.cur_frames * camera * wl.heads * wl.head_dim * 2
