@@ -1,7 +1,7 @@
-// attn_common.cuh - pieces shared by the two segment-attention kernels (one
-// CTA per work item with a BF16 cache; CTA pairs with a one-byte cache): tile
-// sizes, the key-tile walk (dense or block-sparse), the decoding of a work
-// item of the plan, and the softmax / epilogue role of warps 0-7.
+// attn_common.cuh - pieces shared by both forms of the segment-attention
+// kernel (one CTA per work item with a BF16 cache; CTA pairs with a one-byte
+// cache): tile sizes, the key-tile walk (dense or block-sparse), the decoding
+// of a work item of the plan, and the softmax / epilogue role of warps 0-7.
 //
 // What the kernels compute (the "segment-wise causal joint attention" of the
 // madebyagents.com model page over the lifelong KV cache of the orcarouter.ai

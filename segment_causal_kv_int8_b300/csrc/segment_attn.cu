@@ -8,14 +8,18 @@
 // the queries are the current segment's video + text tokens and the keys are
 // the resident cache slots followed by the current segment's own tokens.
 //
-// Design (one CTA = one head x 256 query rows x one key-range split):
+// Design (one CTA = one head x 256 query rows x its whole key range or one
+// piece of it, as the work plan says):
 //   warps 0-3   softmax for query tile 0 (rows   0..127), one thread per row
 //   warps 4-7   softmax for query tile 1 (rows 128..255)
 //   warp  8     TMA producer: Q once, then K/V tiles of 128 keys (into the
-//               ring for a BF16 cache, into int8 staging slots for INT8)
-//   warp  9     TMEM allocator + single-thread tcgen05.mma issuer
+//               4-slot ring for a BF16 cache, into int8 staging slots for INT8)
+//   warp  9     TMEM allocator + tcgen05.mma issuer (one elected lane)
 //   warps 12-15 (INT8 cache) fill the ring: dequantise staged int8 tiles,
 //               fetch current-segment tiles by TMA
+// One-byte caches launch clusters of two CTAs on adjacent query blocks of the
+// same head: each dequantises its 64-row half of every cache tile and copies
+// it into the partner's ring slot, so both see the whole tile.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 f32 columns each; the
 // bf16 probabilities P_t overwrite the first 64 columns of S_t and feed the
 // P.V product straight from tensor memory.  Softmax is online in the log2
