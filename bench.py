@@ -80,6 +80,9 @@ def parse(argv=None):
                     help="override the config's cache format (fp8: the E4M3 comparison variant)")
     ap.add_argument("--camera", type=int, default=0,
                     help="add the camera cross-attention with this many camera tokens per latent frame to the step")
+    ap.add_argument("--bf16-shadow", action="store_true",
+                    help="one-byte caches: expand the resident window to a BF16 copy after the appends "
+                         "(nomas_kvcache_expand) and attend over the copy")
     ap.add_argument("--append-rope", action="store_true",
                     help="write the history with the fused RoPE + append (keys rotated on the way into the cache)")
     ap.add_argument("--sparse", type=float, default=0.0,
@@ -136,6 +139,13 @@ def append_bytes(wl) -> int:
     one_byte = wl.cache_dtype in ("int8", "fp8")
     row = 2 * (wl.head_dim * in_esz + (wl.head_dim + 4 if one_byte else 2 * wl.head_dim))
     return sum(min(f, wl.window) for f in wl.cache_frames_hist) * wl.tpf * wl.heads * row
+
+
+def expand_bytes(wl) -> int:
+    """Algorithmic bytes of the BF16 expansion of the resident window: per row of K and V, the codes
+    and the scale read and the bf16 row written."""
+    resident = min(sum(wl.cache_frames_hist), wl.window) * wl.tpf
+    return 2 * resident * wl.heads * (wl.head_dim + 4 + 2 * wl.head_dim)
 
 
 def rope_bytes(wl) -> int:
@@ -416,9 +426,14 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
     q, k, v = q0.clone(), k0.clone(), v0.clone()
     cache = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames, wl.cache_dtype,
                           device=dev)
+    shadow = None
+    if getattr(args, "bf16_shadow", False) and wl.cache_dtype in ("int8", "fp8"):
+        shadow = nomas.KVCache(1, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames, "bf16",
+                               device=dev)
+    att_cache = shadow if shadow is not None else cache  # the cache the attention reads
     lse = torch.empty((wl.heads, wl.n_q), dtype=torch.float32, device=dev)
     out = torch.empty_like(q)
-    plan = _workspace_plan(nomas, cache, wl, args.num_splits)
+    plan = _workspace_plan(nomas, att_cache, wl, args.num_splits)
     ws = torch.empty(max(plan["workspace_bytes"], 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
@@ -464,6 +479,13 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
                 cache.append(kh, vh)
         if ev is not None:
             ev[1].record(stream)
+        if shadow is not None:
+            if ev is not None:
+                ev[10].record(stream)
+            cache.expand_into(shadow)
+            if ev is not None:
+                ev[11].record(stream)
+        if ev is not None:
             ev[2].record(stream)
         nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, wl.t0, wl.theta, wl.rope_split)
         if ev is not None:
@@ -471,17 +493,17 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
         if keep:
             if ev is not None:
                 ev[6].record(stream)
-            nomas.sparse_select(cache, 0, q, wl.n_video, wl.n_text, keep, tiles=sel_tiles, counts=sel_counts,
+            nomas.sparse_select(att_cache, 0, q, wl.n_video, wl.n_text, keep, tiles=sel_tiles, counts=sel_counts,
                                 workspace=sel_ws)
             if ev is not None:
                 ev[7].record(stream)
         if ev is not None:
             ev[4].record(stream)
         if keep:
-            nomas.segment_attn_sparse(cache, 0, q, k, v, wl.n_video, wl.n_text, sel_tiles, sel_counts, out=out,
-                                      lse=lse, workspace=ws, num_splits=args.num_splits)
+            nomas.segment_attn_sparse(att_cache, 0, q, k, v, wl.n_video, wl.n_text, sel_tiles, sel_counts,
+                                      out=out, lse=lse, workspace=ws, num_splits=args.num_splits)
         else:
-            nomas.segment_attn(cache, 0, q, k, v, wl.n_video, wl.n_text, out=out, lse=lse, workspace=ws,
+            nomas.segment_attn(att_cache, 0, q, k, v, wl.n_video, wl.n_text, out=out, lse=lse, workspace=ws,
                                num_splits=args.num_splits)
         if ev is not None:
             ev[5].record(stream)
@@ -513,7 +535,7 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
 
     import torch.distributed as dist
     sampler = ClockSampler(dev) if with_sampler else None
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(14)] for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -565,14 +587,16 @@ def measure_block_call(args, wl, dev, block, steps, warmup, world, with_sampler=
         "attn_ms": [e[6].elapsed_time(e[7]) for e in evs],
         "select_ms": [e[8].elapsed_time(e[9]) for e in evs] if keep else None,
         "camera_ms": [e[10].elapsed_time(e[11]) for e in evs] if camera else None,
+        "expand_ms": [e[12].elapsed_time(e[13]) for e in evs] if shadow is not None else None,
         "clocks": clocks, "plan": plan, "hist": hist, "qkv": (q_h, k_h, v_h), "steps": steps,
         "append_iso_ms": [e[0].elapsed_time(e[1]) for e in iso],
         "rope_iso_ms": [e[2].elapsed_time(e[3]) for e in iso],
     }
     r["flops"] = sparse_flops(wl, sel_tiles.cpu().numpy(), sel_counts.cpu().numpy()) if keep else wl.attn_flops()
     r["launches_per_step"] = (len(hist) + 1 + 1 + (1 if plan["pieces_per_split_unit"] > 1 else 0)
-                              + (2 if keep and wl.n_cache else 0) + (1 if camera else 0))
-    del cache, hist_d, flush, ws
+                              + (2 if keep and wl.n_cache else 0) + (1 if camera else 0)
+                              + (1 if shadow is not None else 0))
+    del cache, shadow, att_cache, hist_d, flush, ws
     return r
 
 
@@ -593,6 +617,8 @@ def summarize_block_call(wl, m, world, steps, peaks, append_rope=False, camera=0
     el["rope3d"] = hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_ms"]), hbm, 1,
                              isolated=hbm_entry(rope_bytes(wl), 1e3 * statistics.mean(m["rope_iso_ms"]), hbm, 1,
                                                 timing="alone after an L2 eviction"))
+    if m.get("expand_ms"):
+        el["kvcache_expand"] = hbm_entry(expand_bytes(wl), 1e3 * statistics.mean(m["expand_ms"]), hbm, 1)
     if camera:
         nbytes = 2 * wl.n_video * wl.heads * wl.head_dim * 2 + 2 * wl.cur_frames * camera * wl.heads * wl.head_dim * 2
         el["camera_cross_attn"] = hbm_entry(nbytes, 1e3 * statistics.mean(m["camera_ms"]), hbm, 1,
@@ -673,6 +699,9 @@ def run_ours(args):
             line["configs"] = configs
         if args.append_rope:
             line["config"]["workload"] += "; history written by the fused RoPE + append"
+        if args.bf16_shadow and wl.cache_dtype in ("int8", "fp8"):
+            line["config"]["workload"] += ("; the resident window expanded to a BF16 copy after the appends "
+                                           "(nomas_kvcache_expand), attention over the copy")
         if keep:
             # Executed FLOPs count each query group's kept keys; the dense
             # equivalent is the full-attention FLOPs over the same step time.
@@ -717,9 +746,34 @@ def run_extras(args, main_wl, dev, world, peaks):
         s["gpu_launches"] = m["launches_per_step"] * steps
         out[name] = s
         torch.cuda.empty_cache()
+    # The INT8 window with its BF16 copy: once per step here (the step re-appends the history), once
+    # per turn in the session (the copy serves that turn's 8 steps of every block).
+    import copy
+    sh_args = copy.copy(args)
+    sh_args.bf16_shadow = True
+    wl = CONFIGS["c3_int8_window18"]
+    m = measure_block_call(sh_args, wl, dev, rank_block(rank), args.steps, max(3, args.warmup), world,
+                           with_sampler=True, target_s=args.extra_seconds)
+    steps = m["steps"]
+    m["hist"] = m["qkv"] = None
+    total = max_over_ranks(sum(m["step_ms"]), world, dev)
+    s = summarize_block_call(wl, m, world, steps, peaks)
+    s["step"]["ms"] = total / steps
+    s["step"]["whole_job_tflops"] = whole_job_value(m["flops"], world, steps, total)
+    s["clocks"] = m["clocks"]
+    s["gpu_launches"] = m["launches_per_step"] * steps
+    s["note"] = "attention over the BF16 copy of the INT8 window (nomas_kvcache_expand after the appends)"
+    out["c3_int8_window18_bf16_shadow"] = s
+    torch.cuda.empty_cache()
     sess = measure_session(args, CONFIGS[SESSION_CONFIG], dev, world, rank, args.turns, steps=1, warmup=[1],
                            keep=0.0, archive=False)
     out[SESSION_CONFIG] = session_summary(CONFIGS[SESSION_CONFIG], sess, world, peaks)
+    torch.cuda.empty_cache()
+    sess = measure_session(args, CONFIGS[SESSION_CONFIG], dev, world, rank, args.turns, steps=1, warmup=[1],
+                           keep=0.0, archive=False, shadow_bf16=True)
+    ss = session_summary(CONFIGS[SESSION_CONFIG], sess, world, peaks)
+    ss["note"] = "the INT8 window expanded to a BF16 copy of all 54 blocks after each turn's append"
+    out[SESSION_CONFIG + "_bf16_shadow"] = ss
     torch.cuda.empty_cache()
     return out
 
@@ -904,11 +958,12 @@ def session_flops(wl, turns: int, keep: float = 0.0, dense_steps: int = 2) -> fl
     return total
 
 
-def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, archive):
+def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, archive, shadow_bf16=False):
     """Time ``steps`` whole sessions of ``turns`` turns: per turn, steps x blocks calls of RoPE +
     segment attention (each block against its own window of the shared INT8 cache), then one append
     of the finished segment's K/V for all blocks.  ``warmup`` lists the turn counts of the untimed
-    sessions run first."""
+    sessions run first.  ``shadow_bf16``: after each append, expand the window to a BF16 copy of all
+    blocks (nomas_kvcache_expand) and run the next turn's attention over the copy."""
     import ctypes
 
     import torch
@@ -921,6 +976,11 @@ def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, arch
     seed_block = rank_block(rank)
     cache = nomas.KVCache(wl.blocks, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames,
                           wl.cache_dtype, device=dev)
+    shadow = None
+    if shadow_bf16 and wl.cache_dtype in ("int8", "fp8"):
+        shadow = nomas.KVCache(wl.blocks, wl.heads, wl.grid_h, wl.grid_w, wl.capacity_frames, wl.past_frames,
+                               "bf16", device=dev)
+    att_cache = shadow if shadow is not None else cache  # the cache the attention reads
     # A pool of current-segment inputs (values do not change the work) and one
     # finished segment per turn, drawn on the device before timing.
     pool = [current_qkv_torch(wl, seed_block, s, b, dev) for s, b in ((0, 0), (1, 1), (2, 2), (3, 3))]
@@ -928,7 +988,7 @@ def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, arch
     out = torch.empty_like(pool[0][0])
     ws_bytes = 0
     for vf in range(0, wl.window + 1):
-        d = nomas.nomas_kvcache.from_buffer_copy(cache.desc)
+        d = nomas.nomas_kvcache.from_buffer_copy(att_cache.desc)
         d.total_frames, d.valid_frames = vf, vf
         b = ctypes.c_size_t()
         nomas.nomas_segment_attn_workspace_bytes(ctypes.byref(d), wl.n_video, wl.n_text, 0, ctypes.byref(b))
@@ -955,23 +1015,25 @@ def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, arch
 
     def session(n_turns):
         cache.reset(zero_memory=False)
+        if shadow is not None:
+            shadow.reset(zero_memory=False)
         used = 0
         for t in range(n_turns):
             # the plan (and so whether a merge pass follows) depends on the resident frames
-            merge = 1 if cache.attn_plan(wl.n_video, wl.n_text)["pieces_per_split_unit"] > 1 else 0
+            merge = 1 if att_cache.attn_plan(wl.n_video, wl.n_text)["pieces_per_split_unit"] > 1 else 0
             for s in range(wl.steps):
                 for blk in range(wl.blocks):
                     q, k, v = pool[(s * wl.blocks + blk) % len(pool)]
                     nomas.rope3d(q, k, wl.cur_frames, wl.grid_h, wl.grid_w, cache.total_frames, wl.theta,
                                  wl.rope_split)
                     if keep and s >= 2 and cache.valid_frames > 0:
-                        nomas.sparse_select(cache, blk, q, wl.n_video, wl.n_text, keep, tiles=sel_tiles,
+                        nomas.sparse_select(att_cache, blk, q, wl.n_video, wl.n_text, keep, tiles=sel_tiles,
                                             counts=sel_counts, workspace=kbar[blk], reuse_key_means=s > 2)
-                        nomas.segment_attn_sparse(cache, blk, q, k, v, wl.n_video, wl.n_text, sel_tiles, sel_counts,
-                                                  out=out, workspace=ws)
+                        nomas.segment_attn_sparse(att_cache, blk, q, k, v, wl.n_video, wl.n_text, sel_tiles,
+                                                  sel_counts, out=out, workspace=ws)
                         calls[0] += 3 + (1 if s == 2 else 0)
                     else:
-                        nomas.segment_attn(cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
+                        nomas.segment_attn(att_cache, blk, q, k, v, wl.n_video, wl.n_text, out=out, workspace=ws)
                         calls[0] += 1 + merge
                     calls[0] += 1
             if host_archive is not None:
@@ -979,6 +1041,9 @@ def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, arch
             else:
                 cache.append(seg_k, seg_v)
             calls[0] += 1
+            if shadow is not None:
+                cache.expand_into(shadow)
+                calls[0] += 1
 
     for n in warmup:
         session(min(n, turns))
@@ -1000,9 +1065,9 @@ def measure_session(args, wl, dev, world, rank, turns, steps, warmup, keep, arch
         dist.barrier()
     clocks = sampler.stop()
     total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
-    del cache, ws, pool
+    del cache, shadow, att_cache, ws, pool
     return {"total_ms": total_ms, "steps": steps, "turns": turns, "calls": calls[0], "clocks": clocks,
-            "flops": session_flops(wl, turns, keep), "keep": keep, "archive": archive}
+            "flops": session_flops(wl, turns, keep), "keep": keep, "archive": archive, "shadow_bf16": shadow_bf16}
 
 
 def session_summary(wl, s, world, peaks):
@@ -1035,7 +1100,7 @@ def run_session(args):
     wl = CONFIGS[args.config]
     keep = args.sparse
     s = measure_session(args, wl, dev, world, rank, args.turns, args.steps, [args.turns] * args.warmup, keep,
-                        args.archive)
+                        args.archive, shadow_bf16=args.bf16_shadow)
     turns = s["turns"]
     total_ms = s["total_ms"]
     flops = s["flops"]
@@ -1051,6 +1116,7 @@ def run_session(args):
                                    f"window {wl.window} frames), one 54-block append per turn; one step = one session",
                        "turns": turns, "attention_calls": turns * wl.steps * wl.blocks,
                        "host_archive": bool(args.archive),
+                       "bf16_shadow": bool(args.bf16_shadow),
                        "l2": "working set (54 blocks' caches, input pool) far larger than L2",
                        "parallelism": f"replica x{world} (independent sessions per GPU)"},
             "roofline": {"bound": "tensor", "achieved": value / world, "peak": float(peaks["bf16_tflops_sustained"]),

@@ -427,6 +427,27 @@ nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam, const voi
                                      void* out, cudaStream_t stream);
 
 /*
+ * BF16 copy of the resident window of an INT8 or FP8 cache.  The low-memory
+ * preset keeps the cache in INT8 to fit a 24 GB card (Hy-Nomas auf einer RTX
+ * 4090, section "Das Single-GPU-Preset"); the cache changes only when a
+ * finished segment is appended (section "Zeiten"), while every denoising step
+ * of the next segment attends over it.  A caller with memory to spare can
+ * expand the window once per append and run those steps' attention over the
+ * copy (nomas_segment_attn with dst), which gives the same values the
+ * attention kernel dequantises itself: x_hat = bf16(fl32(code * scale)).
+ *
+ *   src  an INT8 or FP8 cache (not modified)
+ *   dst  a BF16 cache of the same geometry (blocks, heads, head_dim, grid,
+ *        capacity_frames, past_frames), buffers distinct from src's; caller-
+ *        owned.  Its resident slots [0, valid_frames * grid_h * grid_w) of
+ *        every (block, head) plane are overwritten, and its total_frames /
+ *        valid_frames are set to src's when the call succeeds.
+ * Stream-ordered, no allocation.  NOMAS_ERR_INVALID_ARG for a BF16 src, a
+ * one-byte dst, mismatched geometry or shared buffers.
+ */
+nomas_status nomas_kvcache_expand(const nomas_kvcache* src, nomas_kvcache* dst, cudaStream_t stream);
+
+/*
  * Start a new session (the resident service's new session_id, "Setup" and the
  * JSON turns on the inferencekey.com RTX 4090 test page): total_frames and
  * valid_frames to 0; with zero_memory != 0 also enqueue a kernel that clears

@@ -118,6 +118,7 @@ EXPORTS = {
                                            _i32, _vp, _vp, _vp, _sz, _i32, _vp]),
     "nomas_camera_cross_attn": (_c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "nomas_kvcache_reset": (_c_int, [_P(nomas_kvcache), _c_int, _vp]),
+    "nomas_kvcache_expand": (_c_int, [_P(nomas_kvcache), _P(nomas_kvcache), _vp]),
     "nomas_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _vp]),
     "nomas_bounds_checked": (_i32, []),
     "nomas_selftest_bounds_check": (_c_int, [_vp]),
@@ -231,6 +232,12 @@ class KVCache:
 
     def nbytes(self) -> int:
         return int(nomas_kvcache_bytes(ctypes.byref(self.desc)))
+
+    def expand_into(self, dst: "KVCache", stream=None) -> None:
+        """Write this one-byte cache's resident window as BF16 values into ``dst`` (a "bf16"
+        KVCache of the same geometry) and give ``dst`` this cache's frame counts."""
+        _check(nomas_kvcache_expand(ctypes.byref(self.desc), ctypes.byref(dst.desc), _stream_ptr(stream)),
+               "nomas_kvcache_expand")
 
     def append(self, k, v, stream=None) -> None:
         """Append a finished segment: ``k``, ``v`` ``[blocks][F*tpf][heads][128]`` (or 3-D for one block)."""

@@ -86,6 +86,24 @@ cudaError_t launch_append(bool f32_in, int kind, const AppendParams& p, int sms,
 cudaError_t launch_append_rope(bool f32_in, int kind, const AppendParams& p, const RopeParams& rp,
                                cudaStream_t stream);
 
+// ------------------------------------------------------------------ BF16 expansion
+// The resident window of a one-byte cache as BF16 values (slots [0, n_slots)
+// of every (block, head) plane).
+struct ExpandParams {
+  const void* kc;                // codes [planes][cap_slots][128]
+  const void* vc;
+  const float* ks;               // scales [planes][cap_slots]
+  const float* vs;
+  void* ko;                      // bf16 [planes][cap_slots][128]
+  void* vo;
+  int planes;                    // blocks * heads
+  long long cap_slots;
+  long long n_slots;             // valid_frames * tpf
+  uint32_t* err;                 // device error word (checked build)
+};
+
+cudaError_t launch_expand(int kind, const ExpandParams& p, cudaStream_t stream);
+
 // ------------------------------------------------------------------ reset
 cudaError_t launch_zero_fill(void* ptr, size_t bytes, cudaStream_t stream);
 

@@ -541,6 +541,38 @@ NOMAS_API nomas_status nomas_camera_cross_attn(const void* q, const void* k_cam,
   return from_cuda(launch_camera_attn(tm, p, stream));
 }
 
+NOMAS_API nomas_status nomas_kvcache_expand(const nomas_kvcache* src, nomas_kvcache* dst, cudaStream_t stream) {
+  nomas_status st = validate_cache(src);
+  if (st != NOMAS_OK) return st;
+  if (dst == nullptr) return NOMAS_ERR_INVALID_ARG;
+  st = validate_cache(dst);
+  if (st != NOMAS_OK) return st;
+  if (!quantised(src) || dst->dtype != NOMAS_BF16) return NOMAS_ERR_INVALID_ARG;
+  if (src->num_blocks != dst->num_blocks || src->heads != dst->heads || src->head_dim != dst->head_dim ||
+      src->grid_h != dst->grid_h || src->grid_w != dst->grid_w || src->capacity_frames != dst->capacity_frames ||
+      src->past_frames != dst->past_frames)
+    return NOMAS_ERR_INVALID_ARG;
+  if (dst->k == src->k || dst->v == src->v || dst->k == dst->v) return NOMAS_ERR_INVALID_ARG;
+  const int64_t tpf = static_cast<int64_t>(src->grid_h) * src->grid_w;
+  ExpandParams p;
+  p.kc = src->k;
+  p.vc = src->v;
+  p.ks = src->k_scale;
+  p.vs = src->v_scale;
+  p.ko = dst->k;
+  p.vo = dst->v;
+  p.planes = src->num_blocks * src->heads;
+  p.cap_slots = tpf * src->capacity_frames;
+  p.n_slots = tpf * src->valid_frames;
+  p.err = nullptr;
+  if (device_state(&p.err, nullptr) != NOMAS_OK) p.err = nullptr;
+  st = from_cuda(launch_expand(cache_kind(src), p, stream));
+  if (st != NOMAS_OK) return st;
+  dst->total_frames = src->total_frames;
+  dst->valid_frames = src->valid_frames;
+  return NOMAS_OK;
+}
+
 NOMAS_API nomas_status nomas_kvcache_reset(nomas_kvcache* cache, int zero_memory, cudaStream_t stream) {
   nomas_status st = validate_cache(cache);
   if (st != NOMAS_OK) return st;

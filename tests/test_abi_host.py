@@ -128,6 +128,29 @@ def test_invalid_calls_return_status_without_launching():
     assert nomas.nomas_kvcache_append(ctypes.byref(d), None, None, nomas.NOMAS_BF16, 0, 0, None) == nomas.NOMAS_OK
 
 
+def test_expand_validates_before_launching():
+    src = _desc(total=2, valid=2)
+
+    def bf16(**kw):
+        d = _desc(dtype=nomas.NOMAS_BF16, **kw)
+        d.k, d.v, d.k_scale, d.v_scale = 4096, 8192, None, None
+        return d
+
+    exp = nomas.nomas_kvcache_expand
+    dst = bf16()
+    # a one-byte destination, a BF16 source, a geometry mismatch, shared buffers
+    assert exp(ctypes.byref(src), ctypes.byref(_desc()), None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert exp(ctypes.byref(bf16(total=2, valid=2)), ctypes.byref(dst), None) == nomas.NOMAS_ERR_INVALID_ARG
+    for kw in (dict(heads=3), dict(gw=5), dict(cap=6), dict(blocks=2)):
+        assert exp(ctypes.byref(src), ctypes.byref(bf16(**kw)), None) == nomas.NOMAS_ERR_INVALID_ARG, kw
+    shared = bf16()
+    shared.k = src.k
+    assert exp(ctypes.byref(src), ctypes.byref(shared), None) == nomas.NOMAS_ERR_INVALID_ARG
+    assert exp(ctypes.byref(src), None, None) == nomas.NOMAS_ERR_INVALID_ARG
+    # nothing failed, so nothing was copied into the destination's metadata
+    assert dst.total_frames == 0 and dst.valid_frames == 0
+
+
 def test_camera_cross_attention_validates_before_launching():
     cam = nomas.nomas_camera_cross_attn
     # frames, grid_h, grid_w, heads, n_cam, scale; fake 256-aligned pointers never reach a launch

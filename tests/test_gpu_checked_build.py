@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_parity.py", "tests/test_gpu_sparse.py", "tests/test_gpu_fp8.py",
           "tests/test_gpu_append_rope.py", "tests/test_gpu_archive.py", "tests/test_gpu_camera.py",
-          "tests/test_gpu_session.py", "tests/test_gpu_resume.py"]
+          "tests/test_gpu_session.py", "tests/test_gpu_resume.py", "tests/test_gpu_expand.py"]
 
 
 def _need_gpu():
