@@ -610,49 +610,76 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint8_t* __restrict__ pt
 // scale, one rounding to bf16).  Eight lanes per 128-value row, 16 codes each:
 // one 16-byte load, two 16-byte stores.  grid.y walks the (tensor, plane)
 // pairs, grid.x and the loop the slots [0, n_slots) of a plane.
+// Converts one 16-code chunk (codes of one row, its scale) to 16 bf16 values.
+template <int K>
+__device__ __forceinline__ void expand_chunk(const uint4& w, float sc, uint32_t (&o)[8]) {
+  if constexpr (K == kCacheFp8) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wd[e] & 0xFFFFu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wd[e] >> 16), __NV_E4M3);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      o[2 * e] = pack_bf16x2(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
+      o[2 * e + 1] = pack_bf16x2(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
+    }
+  } else {
+    // The biased byte c + 128 in the low mantissa bits of 2^23 gives the
+    // float 2^23 + 128 + c; subtracting 2^23 + 128 leaves c exactly.
+    const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float f[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        f[i] = __fmul_rn(__fadd_rn(__uint_as_float(__byte_perm(wd[e], 0x4B000000u, 0x7540u + i)), -8388736.0f), sc);
+      o[2 * e] = pack_bf16x2(f[0], f[1]);
+      o[2 * e + 1] = pack_bf16x2(f[2], f[3]);
+    }
+  }
+}
+
+// BF16 copy of the resident window of a one-byte cache: x_hat = bf16(fl32(code
+// * scale)), the same value the attention kernel's dequantising warps put in
+// shared memory (the code converts exactly, one rounded multiply by the row
+// scale, one rounding to bf16).  Eight lanes per 128-value row, 16 codes each:
+// one 16-byte load, two 16-byte stores; a lane group has the loads of four
+// rows in flight before it converts any.  grid.y walks the (tensor, plane)
+// pairs, grid.x and the loop the slots [0, n_slots) of a plane.
+constexpr int kExpandRows = 4;  // rows in flight per 8-lane group
+
 template <int K>
 __global__ void __launch_bounds__(256) expand_kernel(const __grid_constant__ ExpandParams p) {
   const int c = threadIdx.x & 7;  // 16-code chunk of the row
+  const long long total_rows = static_cast<long long>(p.planes) * p.cap_slots;
   for (long long tp = blockIdx.y; tp < 2LL * p.planes; tp += gridDim.y) {
     const int tensor = tp >= p.planes ? 1 : 0;
     const long long plane = tp - static_cast<long long>(tensor) * p.planes;
-    for (long long slot = static_cast<long long>(blockIdx.x) * 32 + (threadIdx.x >> 3); slot < p.n_slots;
-         slot += static_cast<long long>(gridDim.x) * 32) {
-      const long long slot_row = plane * p.cap_slots + slot;  // row of the cache arrays
-      if (!in_bounds(slot_row, 1, static_cast<long long>(p.planes) * p.cap_slots, p.err)) continue;
-      const uint8_t* codes = static_cast<const uint8_t*>(tensor ? p.vc : p.kc) + slot_row * 128 + 16 * c;
-      const float sc = (tensor ? p.vs : p.ks)[slot_row];
-      const uint4 w = *reinterpret_cast<const uint4*>(codes);
-      uint32_t o[8];
-      if constexpr (K == kCacheFp8) {
-        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    const uint8_t* codes = static_cast<const uint8_t*>(tensor ? p.vc : p.kc);
+    const float* scales = tensor ? p.vs : p.ks;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(tensor ? p.vo : p.ko);
+    for (long long slot0 = (static_cast<long long>(blockIdx.x) * 32 + (threadIdx.x >> 3)) * kExpandRows;
+         slot0 < p.n_slots; slot0 += static_cast<long long>(gridDim.x) * 32 * kExpandRows) {
+      uint4 w[kExpandRows];
+      float sc[kExpandRows];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wd[e] & 0xFFFFu),
-                                                            __NV_E4M3);
-          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wd[e] >> 16), __NV_E4M3);
-          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-          o[2 * e] = pack_bf16x2(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
-          o[2 * e + 1] = pack_bf16x2(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
-        }
-      } else {
-        // The biased byte c + 128 in the low mantissa bits of 2^23 gives the
-        // float 2^23 + 128 + c; subtracting 2^23 + 128 leaves c exactly.
-        const uint32_t wd[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float f[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            f[i] = __fmul_rn(__fadd_rn(__uint_as_float(__byte_perm(wd[e], 0x4B000000u, 0x7540u + i)), -8388736.0f), sc);
-          o[2 * e] = pack_bf16x2(f[0], f[1]);
-          o[2 * e + 1] = pack_bf16x2(f[2], f[3]);
-        }
+      for (int r = 0; r < kExpandRows; ++r) {
+        const long long slot_row = plane * p.cap_slots + slot0 + r;  // row of the cache arrays
+        const bool live = slot0 + r < p.n_slots && in_bounds(slot_row, 1, total_rows, p.err);
+        w[r] = live ? *reinterpret_cast<const uint4*>(codes + slot_row * 128 + 16 * c) : make_uint4(0u, 0u, 0u, 0u);
+        sc[r] = live ? scales[slot_row] : 0.0f;
       }
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(tensor ? p.vo : p.ko) + slot_row * 128 + 16 * c);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+      for (int r = 0; r < kExpandRows; ++r) {
+        const long long slot_row = plane * p.cap_slots + slot0 + r;
+        if (slot0 + r >= p.n_slots || !in_bounds(slot_row, 1, total_rows, p.err)) continue;
+        uint32_t o[8];
+        expand_chunk<K>(w[r], sc[r], o);
+        uint4* dst = reinterpret_cast<uint4*>(out + slot_row * 128 + 16 * c);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
     }
   }
 }
@@ -662,7 +689,7 @@ __global__ void __launch_bounds__(256) expand_kernel(const __grid_constant__ Exp
 cudaError_t launch_expand(int kind, const ExpandParams& p, cudaStream_t stream) {
   if (p.planes <= 0 || p.n_slots <= 0) return cudaSuccess;
   if (kind != kCacheInt8 && kind != kCacheFp8) return cudaErrorInvalidValue;
-  const long long xs = (p.n_slots + 31) / 32;  // 32 rows per 256-thread CTA
+  const long long xs = (p.n_slots + 32 * kExpandRows - 1) / (32 * kExpandRows);  // 32 lane groups per CTA
   const long long tps = 2LL * p.planes;
   const dim3 grid(static_cast<unsigned>(xs < 64 ? xs : 64), static_cast<unsigned>(tps < 65535 ? tps : 65535));
   if (kind == kCacheInt8)
