@@ -143,6 +143,10 @@ nomas_status nomas_kvcache_plan_append(const nomas_kvcache* cache, int32_t n_fra
  *   theta             frequency base (> 0), e.g. 10000
  * Math in float32 (angles reduced with a compensated product), one rounding
  * to io_dt at the end.
+ * NOMAS_ERR_UNSUPPORTED: head_dim != 128, t0 + frames >= 2^24, grid_h or
+ * grid_w >= 2^24, heads > 2^19, n_video > 2^31 - 9.  NOMAS_ERR_INVALID_ARG:
+ * other bad arguments (including q or k not 16-byte aligned, or a row stride
+ * below heads*head_dim or not a multiple of 16 bytes).
  */
 nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, int32_t n_video,
                                 int32_t heads, int32_t head_dim, int64_t row_stride_elems,

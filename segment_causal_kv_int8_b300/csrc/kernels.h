@@ -16,6 +16,8 @@ constexpr int kCacheInt8 = 1;
 constexpr int kCacheFp8 = 2;
 
 constexpr int kRopeMaxPairs = 64;  // head_dim 128 -> 64 rotary pairs
+constexpr int kRopeMaxHeads = 1 << 19;            // heads * 32 vectors per token row stay in int
+constexpr int kRopeMaxVideoRows = 0x7FFFFFFF - 8;  // token index of a CTA's last warp stays in int
 
 // Division by a run-time constant d >= 1 as one multiply and one shift
 // (division by invariant integers, Granlund and Montgomery, PLDI 1994): with

@@ -323,6 +323,7 @@ NOMAS_API nomas_status nomas_rope3d_apply(void* q, void* k, nomas_dtype io_dt, i
   if (!rope_split_ok(theta, d_t, d_h, d_w)) return NOMAS_ERR_INVALID_ARG;
   if (t0 < 0 || t0 + frames >= (int64_t(1) << 24) || grid_h >= (1 << 24) || grid_w >= (1 << 24))
     return NOMAS_ERR_UNSUPPORTED;
+  if (heads > kRopeMaxHeads || n_video > kRopeMaxVideoRows) return NOMAS_ERR_UNSUPPORTED;
   const int64_t esz = io_dt == NOMAS_BF16 ? 2 : 4;
   if (row_stride_elems < static_cast<int64_t>(heads) * head_dim || (row_stride_elems * esz) % 16 != 0)
     return NOMAS_ERR_INVALID_ARG;

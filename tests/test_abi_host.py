@@ -112,6 +112,10 @@ def test_invalid_calls_return_status_without_launching():
     # odd rotary split
     assert nomas.nomas_rope3d_apply(256, None, nomas.NOMAS_BF16, 12, 2, 128, 256, 1, 3, 4, 0, 1e4, 31, 48, 48,
                                     None) == nomas.NOMAS_ERR_INVALID_ARG
+    # more heads than a token row's vector index covers (checked before the row stride)
+    heads = 2 ** 19 + 1
+    assert nomas.nomas_rope3d_apply(256, None, nomas.NOMAS_BF16, 12, heads, 128, heads * 128, 1, 3, 4, 0, 1e4, 32,
+                                    48, 48, None) == nomas.NOMAS_ERR_UNSUPPORTED
     # append: bad dtype, then capacity overflow (checked before any launch)
     assert nomas.nomas_kvcache_append(ctypes.byref(d), 256, 256, 9, 1, 0, None) == nomas.NOMAS_ERR_INVALID_ARG
     assert nomas.nomas_kvcache_append(ctypes.byref(d), 256, 256, nomas.NOMAS_BF16, 6, 0,
