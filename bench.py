@@ -12,7 +12,9 @@ the attention's FLOPs (4 * Nq * Nk * 128 * heads) per step time, in TFLOP/s.
 The headline workload is the 60-frame BF16 history (``c4_bf16_hist60``, the
 largest single-block call).  The same JSON line carries, under ``configs``, the
 other single-block workloads (the INT8 window of 18 frames and the 8-frame
-BF16 history) measured the same way, and one whole simulated 12-turn session
+BF16 history) measured the same way, the INT8 window attended through its BF16
+copy, block-sparse steps keeping a quarter of the cache tiles on the INT8
+window and the 60-frame history, and one whole simulated 12-turn session
 (8 denoising steps x 54 blocks per turn), each with attention TFLOP/s, its
 fraction of the measured dense BF16 peak, query tokens per second per block
 call, and the RoPE / append bandwidth against the measured HBM copy rate and
@@ -46,6 +48,7 @@ UNIT = "TFLOP/s"
 DEFAULT_CONFIG = "c4_bf16_hist60"
 EXTRA_CONFIGS = ("c3_int8_window18", "c2_bf16_hist8")
 SESSION_CONFIG = "c5_session12"
+SPARSE_KEEP = 0.25  # kept fraction of cache tiles in the block-sparse entries
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 HBM_NOMINAL_GBS = 8000.0  # the "about 8 TB/s" HBM figure the RoPE / append targets are quoted against
 
@@ -724,17 +727,17 @@ def run_ours(args):
 def run_extras(args, main_wl, dev, world, peaks):
     """The other single-block workloads (timed like the headline, at least --steps steps and about
     --extra-seconds of device time each) and one whole session, for the ``configs`` key."""
+    import copy
+
     import torch
 
     from synth import CONFIGS
 
     rank, _, _ = dist_env()
     out = {}
-    for name in EXTRA_CONFIGS:
-        if name == main_wl.name:
-            continue
-        wl = CONFIGS[name]
-        m = measure_block_call(args, wl, dev, rank_block(rank), args.steps, max(3, args.warmup), world,
+
+    def block_entry(a, wl):
+        m = measure_block_call(a, wl, dev, rank_block(rank), args.steps, max(3, args.warmup), world,
                                with_sampler=True, target_s=args.extra_seconds)
         steps = m["steps"]
         m["hist"] = m["qkv"] = None
@@ -744,27 +747,31 @@ def run_extras(args, main_wl, dev, world, peaks):
         s["step"]["whole_job_tflops"] = whole_job_value(m["flops"], world, steps, total)
         s["clocks"] = m["clocks"]
         s["gpu_launches"] = m["launches_per_step"] * steps
-        out[name] = s
+        if m["select_ms"]:
+            # executed FLOPs count each query group's kept keys plus the current keys
+            s["sparse"] = {"keep": a.sparse, "select_us": 1e3 * statistics.mean(m["select_ms"]),
+                           "executed_flops": m["flops"], "dense_flops": wl.attn_flops(),
+                           "dense_equivalent_tflops": whole_job_value(wl.attn_flops(), world, steps, total)}
         torch.cuda.empty_cache()
+        return s
+
+    for name in EXTRA_CONFIGS:
+        if name != main_wl.name:
+            out[name] = block_entry(args, CONFIGS[name])
     # The INT8 window with its BF16 copy: once per step here (the step re-appends the history), once
     # per turn in the session (the copy serves that turn's 8 steps of every block).
-    import copy
     sh_args = copy.copy(args)
     sh_args.bf16_shadow = True
-    wl = CONFIGS["c3_int8_window18"]
-    m = measure_block_call(sh_args, wl, dev, rank_block(rank), args.steps, max(3, args.warmup), world,
-                           with_sampler=True, target_s=args.extra_seconds)
-    steps = m["steps"]
-    m["hist"] = m["qkv"] = None
-    total = max_over_ranks(sum(m["step_ms"]), world, dev)
-    s = summarize_block_call(wl, m, world, steps, peaks)
-    s["step"]["ms"] = total / steps
-    s["step"]["whole_job_tflops"] = whole_job_value(m["flops"], world, steps, total)
-    s["clocks"] = m["clocks"]
-    s["gpu_launches"] = m["launches_per_step"] * steps
+    s = block_entry(sh_args, CONFIGS["c3_int8_window18"])
     s["note"] = "attention over the BF16 copy of the INT8 window (nomas_kvcache_expand after the appends)"
     out["c3_int8_window18_bf16_shadow"] = s
-    torch.cuda.empty_cache()
+    # Block-sparse steps (tile selection + tile-list attention) keeping a quarter of the cache tiles.
+    sp_args = copy.copy(args)
+    sp_args.sparse = SPARSE_KEEP
+    for name in ("c3_int8_window18", "c4_bf16_hist60"):
+        s = block_entry(sp_args, CONFIGS[name])
+        s["note"] = f"block-sparse: tile selection, then attention over the kept {SPARSE_KEEP} of the cache tiles"
+        out[f"{name}_sparse{int(round(100 * SPARSE_KEEP))}"] = s
     sess = measure_session(args, CONFIGS[SESSION_CONFIG], dev, world, rank, args.turns, steps=1, warmup=[1],
                            keep=0.0, archive=False)
     out[SESSION_CONFIG] = session_summary(CONFIGS[SESSION_CONFIG], sess, world, peaks)
