@@ -644,10 +644,10 @@ __device__ __forceinline__ void expand_chunk(const uint4& w, float sc, uint32_t 
 // * scale)), the same value the attention kernel's dequantising warps put in
 // shared memory (the code converts exactly, one rounded multiply by the row
 // scale, one rounding to bf16).  Eight lanes per 128-value row, 16 codes each:
-// one 16-byte load, two 16-byte stores; a lane group has the loads of four
+// one 16-byte load, two 16-byte stores; a lane group has the loads of eight
 // rows in flight before it converts any.  grid.y walks the (tensor, plane)
 // pairs, grid.x and the loop the slots [0, n_slots) of a plane.
-constexpr int kExpandRows = 4;  // rows in flight per 8-lane group
+constexpr int kExpandRows = 8;  // rows in flight per 8-lane group
 
 template <int K>
 __global__ void __launch_bounds__(256) expand_kernel(const __grid_constant__ ExpandParams p) {

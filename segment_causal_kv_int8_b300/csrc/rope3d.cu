@@ -54,16 +54,18 @@ __device__ __forceinline__ void rotate_vec(Vec& v, const float (&cc)[kBF16 ? 4 :
 // keeps them in registers.  Up to kTokBatch vectors per lane are loaded before
 // any is rotated; the CTA's first loads go out before it computes the cos/sin
 // table of its tokens.  With two tensors, warps 2t and 2t + 1 take Q and K of
-// token t of the CTA, so both use one table row.
-constexpr int kTokBatch = 8;  // vectors per lane in flight
+// token t of the CTA, so both use one table row.  CTAs are four warps, so a
+// barrier couples few warps and a finished CTA is replaced quickly.
+constexpr int kTokBatch = 8;     // vectors per lane in flight
+constexpr int kTokThreads = 128;  // four warps per CTA
 
 template <bool kBF16, bool kTwo>
-__global__ void __launch_bounds__(256, 4) rope3d_token_kernel(char* __restrict__ q, char* __restrict__ k,
+__global__ void __launch_bounds__(kTokThreads, 8) rope3d_token_kernel(char* __restrict__ q, char* __restrict__ k,
                                                               const __grid_constant__ RopeParams p, TwoPi tp) {
   constexpr int VPR = kBF16 ? 16 : 32;  // vectors per head row
   constexpr int PPV = kBF16 ? 4 : 2;    // rotary pairs per vector
   constexpr int ESZ = kBF16 ? 2 : 4;
-  constexpr int TPC = kTwo ? 4 : 8;     // tokens per CTA
+  constexpr int TPC = kTwo ? 2 : 4;     // tokens per CTA
   using Vec = typename std::conditional<kBF16, uint4, float4>::type;
   __shared__ __align__(16) float2 cs[TPC * 64];  // (cos, sin) of [token of the CTA][pair], interleaved
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(256, 4) rope3d_token_kernel(char* __restrict__
     }
   };
   if (active) load(0);
-  for (int e = tid; e < TPC * 64; e += 256) {
+  for (int e = tid; e < TPC * 64; e += kTokThreads) {
     const int t = e >> 6, pair = e & 63;
     const int a = p.axis[pair];
     const int tk = tok0 + t;
@@ -135,20 +137,20 @@ cudaError_t launch_rope3d(bool bf16_io, void* q, void* k, const RopeParams& p, c
   // vector indices of a token row and token indices of a CTA stay in int
   if (p.heads <= 0 || p.heads > kRopeMaxHeads || p.n_video > kRopeMaxVideoRows) return cudaErrorInvalidValue;
   const TwoPi tp = rope_two_pi();
-  const int tpc = k ? 4 : 8;  // tokens per CTA: Q and K of 4, or Q of 8
+  const int tpc = k ? 2 : 4;  // tokens per CTA: Q and K of 2, or Q of 4
   const unsigned grid = static_cast<unsigned>((p.n_video + tpc - 1) / tpc);
   char* qc = static_cast<char*>(q);
   char* kc = static_cast<char*>(k);
   if (bf16_io) {
     if (k)
-      rope3d_token_kernel<true, true><<<grid, 256, 0, stream>>>(qc, kc, p, tp);
+      rope3d_token_kernel<true, true><<<grid, kTokThreads, 0, stream>>>(qc, kc, p, tp);
     else
-      rope3d_token_kernel<true, false><<<grid, 256, 0, stream>>>(qc, kc, p, tp);
+      rope3d_token_kernel<true, false><<<grid, kTokThreads, 0, stream>>>(qc, kc, p, tp);
   } else {
     if (k)
-      rope3d_token_kernel<false, true><<<grid, 256, 0, stream>>>(qc, kc, p, tp);
+      rope3d_token_kernel<false, true><<<grid, kTokThreads, 0, stream>>>(qc, kc, p, tp);
     else
-      rope3d_token_kernel<false, false><<<grid, 256, 0, stream>>>(qc, kc, p, tp);
+      rope3d_token_kernel<false, false><<<grid, kTokThreads, 0, stream>>>(qc, kc, p, tp);
   }
   return cudaGetLastError();
 }
