@@ -126,10 +126,9 @@ constexpr int kPickThreads = 512;
 // that slot, so no barrier guards the ring.  Items 0 .. 7 are the group's
 // query rows (rows rs + 64 i and rs + 64 i + 32, 16 bytes of each per
 // thread), the items after them the mean keys of 32 tiles each (32 bytes per
-// thread).  Items are requested
-// kPickStages - 1 ahead: the slot refilled is the one the thread read in the
-// step before, and the first mean keys are requested while the last query
-// rows are still being summed.
+// thread).  Items are requested kPickStages - 1 ahead: the slot refilled is
+// the one the thread read in the step before, and the first mean keys are
+// requested while the last query rows are still being summed.
 constexpr int kPickStages = 4;
 constexpr int kPickSlotBytes = 32;
 constexpr int kPickQItems = 512 / 64;  // query items: two rows per thread each
