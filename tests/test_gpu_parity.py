@@ -81,11 +81,10 @@ def test_rope3d_padded_token_rows(io_dtype):
 
 @pytest.mark.parametrize("heads", [8, 32, 64, 65])
 def test_rope3d_head_counts(heads):
-    # 8, 32 and 64 bf16 heads tile the copy ring exactly (8, 2 and 1 tokens per
-    # item: full items skip the per-slot checks, a fill's partial last item
-    # keeps them); 65 heads are wider than one item (the register-streaming
-    # kernel).  2760 video tokens give each CTA a run of about ten tokens, so
-    # full and partial items both occur.  Q and K both rotated, against the oracle.
+    # A warp streams one token row of 16 * heads vectors in batches of 256
+    # (eight per lane): 8 heads fill half a batch, 32 and 64 heads take two and
+    # four full batches, 65 heads five with a ragged last one (16 vectors).
+    # 2760 video tokens on a 23 x 40 grid; Q and K both rotated, against the oracle.
     wl = small_variant(CONFIGS["c2_bf16_hist8"], heads=heads, grid_h=23, grid_w=40, cur_frames=3, n_text=5,
                        seed=90 + heads)
     q, k, _ = current_qkv(wl)
